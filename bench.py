@@ -1,0 +1,442 @@
+"""Benchmark of the attention forward pass (TFLOP/s, one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llm_prefill|long_sequence|max_shift|ragged_causal|tiny]
+
+A step is one attention forward over the whole workload (all heads, all
+query tiles). ``value`` is whole-job TFLOP/s (4·B·H·N²·d per step, halved
+under the causal mask, summed over ranks) with inputs already in HBM, timed
+with CUDA events over exactly K steps between barriers (max over ranks).
+``e2e`` is the same metric with the inputs copied from pinned host memory
+and O/LSE copied back inside the timed region, through the same C ABI call.
+``roofline`` relates the kernel's average launch time to the measured dense
+bf16 tensor peak; ``cpu_baseline`` is the fp64 oracle on the host cores over a
+bounded sample of query rows.
+
+``--impl reference`` times the oracle instead (rank 0 only), on the same
+workload, over a bounded sample of rows per step.
+
+Multi-GPU (torchrun): each rank runs its own independent batch (seeded by
+rank); no collective touches the data path ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_attention_91_gb300 import inputs as fin  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_BF16_TFLOPS = 1900.0
+METRIC = "attention fwd TFLOP/s and % of GB300 dense-bf16 peak at 1 GPU"
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the forward
+# kernel, from the ncu capture summarised under profiles/ (the file named in
+# "source"), valid only while the kernel sources hash to "kernel_sha".
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_91_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    try:
+        with open(TRAFFIC_FILE, encoding="utf-8") as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = t.get(workload)
+    if not ent or ent.get("kernel_sha") != kernel_sha():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json"), encoding="utf-8") as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background; samples carry the
+    host time they were read at so the timed region can be picked out."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,pci.bus_id")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.bus_id and self.bus_id not in parts[8].lower() and parts[8].lower() not in self.bus_id:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "during timed region"
+        if not inside:
+            after = [p for (t, p) in self.samples if t > t1][:2]
+            before = [p for (t, p) in self.samples if t < t0][-2:]
+            inside = before + after
+            note = "timed region shorter than the sampling period: nearest samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[4 + i].lower().startswith("active")})
+        power = [num(p[2]) for p in inside if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "power_w_max": max(power) if power else None,
+                "note": note}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo", encoding="utf-8") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def row_flops(w: fin.Workload, rows: np.ndarray) -> float:
+    """Algorithmic flops of the given flat query rows: 4·d per visible key."""
+    if w.causal:
+        keys = (rows % w.N) + 1
+        return float(4.0 * w.d * keys.sum())
+    return float(4.0 * w.d * w.N * len(rows))
+
+
+def oracle_sample(w: fin.Workload, x: fin.Inputs, target_s: float, seed: int):
+    """Times the oracle on a bounded random sample of rows, sized to take
+    about target_s seconds. Returns (flops, seconds, n_rows, heads, threads)."""
+    import oracle
+    oracle.build()
+    g = np.random.Generator(np.random.PCG64(seed))
+    BH = w.B * w.H
+    heads = np.unique(g.integers(0, BH, size=min(BH, 4)))
+    qh = fin.bf16_to_f64(x.q.reshape(BH, w.N, w.d)[heads])[None]
+    kh = fin.bf16_to_f64(x.k.reshape(BH, w.N, w.d)[heads])[None]
+    vh = fin.bf16_to_f64(x.v.reshape(BH, w.N, w.d)[heads])[None]
+    n_local = len(heads) * w.N
+    # calibrate on a small sample, then size the measured one
+    probe = g.integers(0, n_local, size=min(n_local, 64))
+    t = time.perf_counter()
+    oracle.attn_rows(qh, kh, vh, probe, w.scale, w.causal)
+    dt = max(time.perf_counter() - t, 1e-6)
+    per_flop = dt / max(row_flops(w, probe), 1.0)
+    rows = probe
+    while True:
+        n = int(min(n_local, max(64, len(rows) * 2)))
+        rows = g.integers(0, n_local, size=n)
+        if row_flops(w, rows) * per_flop >= target_s or n >= n_local:
+            break
+    t = time.perf_counter()
+    oracle.attn_rows(qh, kh, vh, rows, w.scale, w.causal)
+    dt = time.perf_counter() - t
+    return row_flops(w, rows), dt, len(rows), len(heads), oracle.host_threads()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, w: fin.Workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    x = fin.make_inputs(w)
+    per_step_s = max(0.5, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    flops_total = 0.0
+    secs_total = 0.0
+    rows_n = heads_n = threads = 0
+    for i in range(args.warmup + args.steps):
+        f, s, rows_n, heads_n, threads = oracle_sample(w, x, per_step_s, seed=w.seed + 17 * i)
+        if i >= args.warmup:
+            flops_total += f
+            secs_total += s
+    value = flops_total / secs_total / 1e12
+    sample = (f"{rows_n} random query rows per step from {heads_n} heads of the {w.name} workload "
+              f"(~{per_step_s:.1f} s of fp64 CPU work per step); host CPU {cpu_model()}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs_total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w: fin.Workload, world: int) -> dict:
+    ws = 4 * w.B * w.H * w.N * w.d * 2
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "values": w.values, "scale": w.scale, "seed": w.seed,
+            "parallelism": f"independent batches x{world}" if world > 1 else "single GPU",
+            "l2": ("inputs larger than L2" if ws > 2 * L2_BYTES else "L2 flushed between timed launches")}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, w: fin.Workload):
+    import torch
+    import exact_attention_91_gb300 as fa
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", rank=rank, world_size=world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.load_library()
+
+    wr = w if world == 1 else fin.Workload(w.name, w.B, w.H, w.N, w.d, w.causal, w.values,
+                                           w.seed + 1000 * rank)
+    x = fin.make_inputs(wr)
+
+    def up(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v = up(x.q), up(x.k), up(x.v)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    B, H, N, d = w.B, w.H, w.N, w.d
+
+    def launch():
+        rc = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       B, H, N, d, w.scale, w.causal, sp)
+        if rc != 0:
+            raise fa.FaError(rc)
+
+    working_set = 4 * B * H * N * d * 2
+    flush = None if working_set > 2 * L2_BYTES else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    bus = None
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}"
+    except AttributeError:
+        pass
+    sampler = ClockSampler(bus)
+    sampler.start()
+    time.sleep(0.3)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 0)):
+            launch()
+            if flush is not None:
+                flush.zero_()
+    stream.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        t_begin.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+            if flush is not None:
+                flush.zero_()
+        t_end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier()
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = sum(launch_ms)
+    region_ms = t_begin.elapsed_time(t_end)
+    # with an L2 flush between launches the flush is not part of the work
+    step_total_ms = kernel_ms if flush is not None else region_ms
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([step_total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_total_ms = float(t.item())
+    clocks = sampler.summary(wall0, wall1)
+
+    # ---- end to end: pinned host buffers, copies inside the timed region
+    hq = torch.from_numpy(x.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(x.k.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(x.v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        launch()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+    with torch.cuda.stream(stream):
+        e2e_step()
+    stream.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    sampler.stop()
+
+    flops_step = w.flops
+    value = world * args.steps * flops_step / (step_total_ms * 1e-3) / 1e12
+    e2e_value = world * e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
+    avg_launch_s = kernel_ms / args.steps * 1e-3
+    achieved = flops_step / avg_launch_s / 1e12
+    peaks = load_peaks()
+    if peaks and peaks.get("bf16_tflops"):
+        peak, peak_src = float(peaks["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    else:
+        peak, peak_src = FALLBACK_BF16_TFLOPS, "fallback"
+    traffic = load_traffic(w.name)
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        f, s, n_rows, n_heads, threads = oracle_sample(w, x, args.cpu_seconds, seed=w.seed + 5)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": (f"{n_rows} random query rows from {n_heads} heads of the {w.name} workload, "
+                          f"{s:.1f} s of fp64 CPU work; host CPU {cpu_model()}")}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, world),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "kernel": "fa_fwd", "flops_per_launch": flops_step,
+                     "avg_launch_ms": avg_launch_s * 1e3},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 3 * B * H * N * d * 2,
+                "d2h_bytes_per_step": B * H * N * d * 2 + B * H * N * 4, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(fin.WORKLOADS), default="llm_prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    w = fin.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

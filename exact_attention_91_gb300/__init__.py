@@ -1,0 +1,117 @@
+"""Python binding of libfa.so, the GB300 (sm_103a) exact-attention forward.
+
+The C entry points (``include/fa.h``) are exposed under the same names and
+take raw device pointers (ints), exactly like the C ABI. ``attention_forward``
+is a convenience wrapper for torch tensors: it checks dtypes and layout,
+allocates the outputs with torch and calls ``fa_fwd`` on the current stream.
+Every step of the computation runs in the CUDA library; if the library is
+missing this module raises instead of computing anything elsewhere.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from .build import LIB_PATH
+
+__all__ = ["FaError", "load_library", "fa_fwd", "fa_strerror", "fa_device_status",
+           "fa_set_wait_limit_ns", "fa_abi_version", "attention_forward", "EXPORTED_SYMBOLS"]
+
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_strerror", "fa_device_status", "fa_set_wait_limit_ns",
+                    "fa_abi_version")
+
+FA_OK = 0
+FA_ERR_DEVICE_TIMEOUT = -8
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str = "fa_fwd"):
+        self.status = status
+        super().__init__(f"{what} failed: {status} ({fa_strerror(status)})")
+
+
+def load_library(path: str | None = None):
+    """Loads libfa.so (built in-tree by ``exact_attention_91_gb300.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise FileNotFoundError(
+            f"{p} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+    lib = ctypes.CDLL(p)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_strerror.argtypes = [i]
+    lib.fa_strerror.restype = ctypes.c_char_p
+    lib.fa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.fa_device_status.restype = i
+    lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.fa_set_wait_limit_ns.restype = None
+    lib.fa_abi_version.argtypes = []
+    lib.fa_abi_version.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def fa_fwd(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, N: int, d: int,
+           scale: float, causal: bool, stream: int | None) -> int:
+    """The C ``fa_fwd``: device pointers as ints, returns the status code."""
+    return load_library().fa_fwd(q, k, v, o, lse or None, B, H, N, d, scale, int(bool(causal)),
+                                 stream or None)
+
+
+def fa_strerror(status: int) -> str:
+    return load_library().fa_strerror(status).decode()
+
+
+def fa_device_status(stream: int | None = None) -> tuple[int, int]:
+    """Synchronises ``stream``, reads and clears the device status word."""
+    bits = ctypes.c_uint(0)
+    rc = load_library().fa_device_status(stream or None, ctypes.byref(bits))
+    return rc, bits.value
+
+
+def fa_set_wait_limit_ns(ns: int) -> None:
+    load_library().fa_set_wait_limit_ns(ns)
+
+
+def fa_abi_version() -> int:
+    return load_library().fa_abi_version()
+
+
+def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                      return_lse: bool = True, stream=None):
+    """O (bf16) and LSE (fp32) for bf16 CUDA tensors q, k, v of shape [B, H, N, d].
+
+    ``out`` / ``lse`` may be given to reuse buffers. Runs on ``stream`` (a
+    torch.cuda.Stream) or the current stream.
+    """
+    import torch
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k, v must be bf16")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [B, H, N, d]")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale), causal,
+                s.cuda_stream)
+    if rc != FA_OK:
+        raise FaError(rc)
+    return (out, lse) if return_lse else out

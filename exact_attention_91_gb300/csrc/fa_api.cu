@@ -1,0 +1,210 @@
+// C ABI of libfa.so: argument checks, TMA tensor maps, kernel selection and
+// launch. Declarations and the contract of every entry point are in fa.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "fa_fwd_simple.cuh"
+
+namespace {
+
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
+
+struct DeviceState {
+    bool probed = false;
+    int status = FA_OK;  // FA_OK, FA_ERR_UNSUPPORTED_ARCH
+    int sm_count = 0;
+};
+DeviceState g_devices[kMaxDevices];
+
+int resolve_encode() {
+    if (g_encode) return FA_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return FA_ERR_LAUNCH;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return FA_OK;
+}
+
+// Checks the current device once: it must be compute capability 10.3.
+int probe_device(int* dev_out, DeviceState** st_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return FA_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& st = g_devices[dev];
+    if (!st.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_NO_DEVICE;
+        }
+        st.status = (major == 10 && minor == 3) ? FA_OK : FA_ERR_UNSUPPORTED_ARCH;
+        st.sm_count = sms;
+        st.probed = true;
+    }
+    if (st.status == FA_OK) {
+        int rc = resolve_encode();
+        if (rc != FA_OK) return rc;
+    }
+    *dev_out = dev;
+    *st_out = &st;
+    return st.status;
+}
+
+// 3-D view [B*H][N][d] of a contiguous bf16 [B,H,N,d] tensor, boxes of
+// 128 rows x 64 columns (128 bytes, 128-byte swizzle). Rows past N inside a
+// head read as zero and are not written by stores.
+int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(fa::kBoxCols), static_cast<cuuint32_t>(fa::kBlockM), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+template <int D, bool CAUSAL>
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+           const fa::FwdParams& prm, int dev, cudaStream_t stream) {
+    using Cfg = fa::SimpleCfg<D, true>;
+    auto kernel = fa::fa_fwd_simple_kernel<D, CAUSAL, true>;
+    // At least 92 KB per CTA keeps two CTAs per SM, so their TMEM (256
+    // columns each) always fits the SM's 512 columns.
+    const int smem = Cfg::kSmemBytes > 92 * 1024 ? Cfg::kSmemBytes : 92 * 1024;
+    static bool attr_set[kMaxDevices] = {};
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+                cudaGetLastError();
+                return FA_ERR_LAUNCH;
+            }
+            attr_set[dev] = true;
+        }
+    }
+    const unsigned grid = static_cast<unsigned>(prm.num_q_tiles) * static_cast<unsigned>(prm.num_heads_total);
+    kernel<<<grid, Cfg::kThreads, smem, stream>>>(tq, tk, tv, to, prm);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_abi_version(void) { return FA_ABI_VERSION; }
+
+const char* fa_strerror(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_NULL_PTR: return "q, k, v or o is a null pointer";
+        case FA_ERR_BAD_SHAPE: return "B, H and N must be >= 1 and within the size limits";
+        case FA_ERR_UNSUPPORTED_HEAD_DIM: return "head dimension d must be 64 or 128";
+        case FA_ERR_MISALIGNED: return "q, k, v, o must be 16-byte aligned and lse 4-byte aligned";
+        case FA_ERR_NO_DEVICE: return "no usable CUDA device";
+        case FA_ERR_UNSUPPORTED_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
+        case FA_ERR_LAUNCH: return "tensor-map encoding or kernel launch failed";
+        case FA_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on an mbarrier";
+        case FA_ERR_BAD_SCALE: return "scale must be finite and > 0";
+        case FA_ERR_ALIAS: return "an output buffer overlaps an input buffer or the other output";
+        default: return "unknown fa status";
+    }
+}
+
+void fa_set_wait_limit_ns(unsigned long long ns) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_wait_limit_ns = ns ? ns : kDefaultWaitLimitNs;
+}
+
+int fa_device_status(void* stream, unsigned* bits) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_NO_DEVICE;
+    }
+    unsigned word = 0;
+    const unsigned zero = 0;
+    if (cudaMemcpyFromSymbol(&word, fa::g_status, sizeof(word)) != cudaSuccess ||
+        cudaMemcpyToSymbol(fa::g_status, &zero, sizeof(zero)) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_LAUNCH;
+    }
+    if (bits) *bits = word;
+    return word ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, float scale,
+           int causal, void* stream) {
+    if (!q || !k || !v || !o) return FA_ERR_NULL_PTR;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long n_q_tiles = (static_cast<long long>(N) + fa::kBlockM - 1) / fa::kBlockM;
+    if (BH > 0x7fffffffLL || BH * n_q_tiles > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEAD_DIM;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_MISALIGNED;
+    const size_t tensor_bytes = static_cast<size_t>(BH) * N * d * 2;
+    const size_t lse_bytes = static_cast<size_t>(BH) * N * 4;
+    if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
+        overlaps(o, tensor_bytes, v, tensor_bytes))
+        return FA_ERR_ALIAS;
+    if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
+                overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, o, tensor_bytes)))
+        return FA_ERR_ALIAS;
+
+    int dev = -1;
+    DeviceState* st = nullptr;
+    int rc = probe_device(&dev, &st);
+    if (rc != FA_OK) return rc;
+
+    CUtensorMap tq, tk, tv, to;
+    const int bh = static_cast<int>(BH);
+    if (encode_map(&tq, q, bh, N, d) != FA_OK || encode_map(&tk, k, bh, N, d) != FA_OK ||
+        encode_map(&tv, v, bh, N, d) != FA_OK || encode_map(&to, o, bh, N, d) != FA_OK)
+        return FA_ERR_LAUNCH;
+
+    fa::FwdParams prm{};
+    prm.lse = lse;
+    prm.N = N;
+    prm.num_heads_total = bh;
+    prm.num_q_tiles = static_cast<int>(n_q_tiles);
+    prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        prm.wait_limit_ns = g_wait_limit_ns;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d == 64) return causal ? launch<64, true>(tq, tk, tv, to, prm, dev, s) : launch<64, false>(tq, tk, tv, to, prm, dev, s);
+    return causal ? launch<128, true>(tq, tk, tv, to, prm, dev, s) : launch<128, false>(tq, tk, tv, to, prm, dev, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) exact-attention forward library
+ * (libfa.so).
+ *
+ * The operation is exact softmax attention computed tile by tile with the
+ * online softmax, never writing the N×N score matrix to memory:
+ *
+ *   S = scale · Q Kᵀ,   causal: S[i, j] = -inf for j > i
+ *   P = softmax(S) by rows
+ *   O = P V,            LSE_i = ln Σ_j exp(S[i, j])
+ *
+ * Definition: "Mini FlashAttention", §1 "What attention is" (the three-line
+ * math and the causal-mask sentence). Streaming form: "Mini FlashAttention",
+ * §4 "The flash trick: online softmax" (running max, running sum, rescale of
+ * the running output, O = acc / l after the last chunk); "How Did I Write My
+ * First FlashAttention Kernel in CUDA?", the pseudo-algorithm steps 1-5 and the
+ * surrogate running-output paragraph. Initialisation and final normalisation:
+ * the grasp.study lesson on the complete forward pass, "1. Initialization" and
+ * "3. Finalization".
+ *
+ * Plain C types only: device pointers are `const void*` / `void*`, the CUDA
+ * stream is passed as `void*` (a cudaStream_t; NULL is the legacy default
+ * stream). No function allocates device memory.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. 0 is success; every error is negative. */
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_NULL_PTR = -1,             /* q, k, v or o is NULL */
+    FA_ERR_BAD_SHAPE = -2,            /* B, H or N < 1, or a size past the limits below */
+    FA_ERR_UNSUPPORTED_HEAD_DIM = -3, /* d is not 64 or 128 */
+    FA_ERR_MISALIGNED = -4,           /* q, k, v, o not 16-byte aligned, or lse not 4-byte aligned */
+    FA_ERR_NO_DEVICE = -5,            /* no CUDA device, or the current device cannot be queried */
+    FA_ERR_UNSUPPORTED_ARCH = -6,     /* the current device is not compute capability 10.3 */
+    FA_ERR_LAUNCH = -7,               /* tensor-map encoding or the kernel launch failed */
+    FA_ERR_DEVICE_TIMEOUT = -8,       /* a kernel gave up waiting on an mbarrier (see fa_device_status) */
+    FA_ERR_BAD_SCALE = -9,            /* scale is not finite, or not > 0 */
+    FA_ERR_ALIAS = -10                /* o or lse overlaps q, k or v, or lse overlaps o */
+} fa_status;
+
+/*
+ * fa_fwd — attention forward pass on the current CUDA device.
+ *
+ * q, k, v  device, bf16, contiguous [B, H, N, d] (row-major: d fastest).
+ *          Read only.
+ * o        device, bf16, contiguous [B, H, N, d]. Written: O = P V.
+ * lse      device, fp32, contiguous [B, H, N], or NULL to skip it. Written:
+ *          the natural-log log-sum-exp of each query row's scaled scores
+ *          over the keys the row may see.
+ * B, H, N  batch, heads, sequence length (queries = keys = N), each >= 1;
+ *          B*H <= 2^31-1 and ceil(N/128)*B*H <= 2^31-1.
+ * d        head dimension: 64 or 128.
+ * scale    score scale (the pages use 1/sqrt(d)); finite and > 0.
+ * causal   nonzero: key j is hidden from query i when j > i (top-left
+ *          aligned; every row keeps at least its own key).
+ * stream   cudaStream_t to run on, as void*; NULL = legacy default stream.
+ *
+ * Ownership: the caller allocates and owns every buffer; the library keeps
+ * no pointer after the call returns. The call is asynchronous: argument errors
+ * are returned before anything is queued; faults inside the kernel appear at
+ * the caller's next synchronisation, and a kernel that gave up on a wait
+ * leaves its O/LSE rows unwritten and reports through fa_device_status().
+ * The current device must be compute capability 10.3 (sm_103a).
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/* Static English text for a return code (never NULL). */
+const char* fa_strerror(int status);
+
+/*
+ * fa_device_status — synchronises `stream` (a cudaStream_t as void*, NULL =
+ * legacy default), then reads and clears the current device's status word.
+ * Returns FA_OK if no kernel gave up on a wait since the last call,
+ * FA_ERR_DEVICE_TIMEOUT if one did (then *bits, if not NULL, receives the
+ * word: which kind of wait gave up), or FA_ERR_NO_DEVICE / FA_ERR_LAUNCH if
+ * the synchronisation or the read failed.
+ */
+int fa_device_status(void* stream, unsigned* bits);
+
+/*
+ * fa_set_wait_limit_ns — how long a kernel waits on one mbarrier phase before
+ * giving up (default 2e9 ns). Applies to launches made after the call, on
+ * every device. 0 restores the default.
+ */
+void fa_set_wait_limit_ns(unsigned long long ns);
+
+/* ABI version of this header (bumped on any incompatible change). */
+int fa_abi_version(void);
+
+#define FA_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,81 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+that include/fa.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+import exact_attention_91_gb300 as fa
+from exact_attention_91_gb300 import build as fa_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fa.h")
+
+
+def _declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_ ]+\**\s*\**\s*(fa_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not fa_build.up_to_date():
+        if shutil.which(fa_build.nvcc_path()) is None and not os.path.exists(fa_build.nvcc_path()):
+            pytest.skip("nvcc not available to build libfa.so")
+        fa_build.build()
+    return fa.load_library()
+
+
+def test_header_declares_the_entry_points():
+    assert _declared_functions() == sorted(fa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert fa.fa_abi_version() == 1
+
+
+def test_strerror_covers_every_code(lib):
+    for code in range(0, -11, -1):
+        msg = fa.fa_strerror(code)
+        assert msg and "unknown" not in msg
+    assert "unknown" in fa.fa_strerror(-99)
+
+
+P = 1 << 20  # a 16-byte-aligned fake address; never dereferenced by these calls
+
+
+def _call(q=P, k=2 * P, v=3 * P, o=4 * P, lse=5 * P, B=1, H=1, N=128, d=64, scale=0.125,
+          causal=0):
+    return fa.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), -1), (dict(k=0), -1), (dict(v=0), -1), (dict(o=0), -1),
+    (dict(B=0), -2), (dict(H=0), -2), (dict(N=0), -2), (dict(N=-5), -2),
+    (dict(B=1 << 16, H=1 << 16), -2),
+    (dict(d=32), -3), (dict(d=96), -3), (dict(d=256), -3),
+    (dict(q=P + 8), -4), (dict(o=4 * P + 2), -4), (dict(lse=5 * P + 2), -4),
+    (dict(scale=0.0), -9), (dict(scale=-1.0), -9), (dict(scale=float("inf")), -9),
+    (dict(scale=float("nan")), -9),
+    (dict(o=P), -10), (dict(o=P + 64 * 128), -10), (dict(lse=4 * P + 16), -10),
+])
+def test_bad_arguments_are_rejected_before_launch(lib, kw, code):
+    assert _call(**kw) == code
+
+
+def test_valid_call_without_gpu_reports_no_device(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call() == -5
+    assert _call(lse=0) == -5
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(FileNotFoundError):
+        fa.load_library(str(tmp_path / "libfa.so"))
