@@ -11,6 +11,8 @@
 
 #include "fa.h"
 #include "fa_fwd_simple.cuh"
+#include "fa_fwd_ws.cuh"
+#include <cstdlib>
 
 namespace {
 
@@ -93,12 +95,10 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 template <int D, bool CAUSAL>
-int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-           const fa::FwdParams& prm, int dev, cudaStream_t stream) {
+int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                  const fa::FwdParams& prm, int dev, cudaStream_t stream) {
     using Cfg = fa::SimpleCfg<D, true>;
     auto kernel = fa::fa_fwd_simple_kernel<D, CAUSAL, true>;
-    // At least 92 KB per CTA keeps two CTAs per SM, so their TMEM (256
-    // columns each) always fits the SM's 512 columns.
     const int smem = Cfg::kSmemBytes > 92 * 1024 ? Cfg::kSmemBytes : 92 * 1024;
     static bool attr_set[kMaxDevices] = {};
     {
@@ -114,6 +114,44 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
     const unsigned grid = static_cast<unsigned>(prm.num_q_tiles) * static_cast<unsigned>(prm.num_heads_total);
     kernel<<<grid, Cfg::kThreads, smem, stream>>>(tq, tk, tv, to, prm);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+// Persistent warp-specialised kernel: one CTA per SM (its shared memory and
+// all 512 TMEM columns keep it alone on the SM), looping over work units of
+// one head x 256 query rows.
+template <int D, bool CAUSAL>
+int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+              const fa::FwdParams& prm, int dev, int sm_count, cudaStream_t stream) {
+    using Cfg = fa::WsCfg<D>;
+    auto kernel = fa::fa_fwd_ws_kernel<D, CAUSAL>;
+    static bool attr_set[kMaxDevices] = {};
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return FA_ERR_LAUNCH;
+            }
+            attr_set[dev] = true;
+        }
+    }
+    const long long nqb = (static_cast<long long>(prm.N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+    const long long units = nqb * prm.num_heads_total;
+    const unsigned grid = static_cast<unsigned>(units < sm_count ? units : sm_count);
+    kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+template <int D, bool CAUSAL>
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+           const fa::FwdParams& prm, int dev, int sm_count, cudaStream_t stream) {
+    static const bool use_simple = [] {
+        const char* e = std::getenv("FA_KERNEL");
+        return e != nullptr && e[0] == 's';
+    }();
+    if (use_simple) return launch_simple<D, CAUSAL>(tq, tk, tv, to, prm, dev, stream);
+    return launch_ws<D, CAUSAL>(tq, tk, tv, to, prm, dev, sm_count, stream);
 }
 
 }  // namespace
@@ -203,8 +241,11 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         prm.wait_limit_ns = g_wait_limit_ns;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (d == 64) return causal ? launch<64, true>(tq, tk, tv, to, prm, dev, s) : launch<64, false>(tq, tk, tv, to, prm, dev, s);
-    return causal ? launch<128, true>(tq, tk, tv, to, prm, dev, s) : launch<128, false>(tq, tk, tv, to, prm, dev, s);
+    const int sms = st->sm_count;
+    if (d == 64)
+        return causal ? launch<64, true>(tq, tk, tv, to, prm, dev, sms, s) : launch<64, false>(tq, tk, tv, to, prm, dev, sms, s);
+    return causal ? launch<128, true>(tq, tk, tv, to, prm, dev, sms, s)
+                  : launch<128, false>(tq, tk, tv, to, prm, dev, sms, s);
 }
 
 }  // extern "C"

@@ -44,7 +44,7 @@ __device__ unsigned int g_status;
 // Slow path of a bounded wait: polls the barrier, and every few probes checks
 // the CTA's abort flag, the device status word (another CTA gave up) and the
 // elapsed time. On giving up it records `site` and raises the CTA abort flag.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* cta_abort,
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* cta_abort,
                                        unsigned site, unsigned long long limit_ns) {
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -74,7 +74,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 // Final drain before TMEM is freed: waits for an mbarrier phase with a short
 // limit of its own, ignoring the abort flag (the point is to let any MMA still
 // in flight finish even after the CTA gave up on something else).
-__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (ptx::mbar_try_wait(bar, parity)) return true;

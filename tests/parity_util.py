@@ -6,9 +6,10 @@ mean |Δ| ≤ 1e-3 over the compared elements; LSE max |Δ| ≤ 1e-3.
 
 For shapes with very few keys per query (N = 2, say) each O row is an average
 of one or two V rows, so |O| is O(1) and the bf16 rounding of the exact O by
-itself costs close to 1e-3 on average. Those extra shapes are held to 1e-3 on
-top of that rounding floor (``rounding_floor=True``); the named workloads are
-held to the plain 1e-3.
+itself costs close to 1e-3 on average (and up to a bf16 half-ulp of |O| ≈ 2-3,
+about 8e-3, at worst). Those extra shapes are held to the bars on top of that
+rounding floor (``rounding_floor=True``); the named workloads are held to the
+plain bars.
 """
 from __future__ import annotations
 
@@ -56,6 +57,7 @@ def compare(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: 
         "o_max_abs": float(d_o.max()),
         "o_mean_abs": float(d_o.mean()),
         "o_mean_abs_rounding_only": float(np.abs(o_ref_bf16 - o_ref).mean()),
+        "o_max_abs_rounding_only": float(np.abs(o_ref_bf16 - o_ref).max()),
         "lse_max_abs": float(d_l.max()),
         "finite": bool(np.isfinite(o_gpu).all() and np.isfinite(lse_gpu).all()),
     }
@@ -65,7 +67,8 @@ def compare(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: 
 
 def assert_within(stats: dict, rounding_floor: bool = False) -> None:
     assert stats["finite"], stats
-    assert stats["o_max_abs"] <= O_MAX_ABS, stats
+    max_bar = O_MAX_ABS + (stats["o_max_abs_rounding_only"] if rounding_floor else 0.0)
+    assert stats["o_max_abs"] <= max_bar, stats
     mean_bar = O_MEAN_ABS + (stats["o_mean_abs_rounding_only"] if rounding_floor else 0.0)
     assert stats["o_mean_abs"] <= mean_bar, stats
     assert stats["lse_max_abs"] <= LSE_MAX_ABS, stats
