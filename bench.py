@@ -180,34 +180,44 @@ def row_flops(w: fin.Workload, rows: np.ndarray) -> float:
     return float(4.0 * w.d * w.N * len(rows))
 
 
-def oracle_sample(w: fin.Workload, x: fin.Inputs, target_s: float, seed: int):
-    """Times the oracle on a bounded random sample of rows, sized to take
-    about target_s seconds. Returns (flops, seconds, n_rows, heads, threads)."""
-    import oracle
-    oracle.build()
-    g = np.random.Generator(np.random.PCG64(seed))
-    BH = w.B * w.H
-    heads = np.unique(g.integers(0, BH, size=min(BH, 4)))
-    qh = fin.bf16_to_f64(x.q.reshape(BH, w.N, w.d)[heads])[None]
-    kh = fin.bf16_to_f64(x.k.reshape(BH, w.N, w.d)[heads])[None]
-    vh = fin.bf16_to_f64(x.v.reshape(BH, w.N, w.d)[heads])[None]
-    n_local = len(heads) * w.N
-    # calibrate on a small sample, then size the measured one
-    probe = g.integers(0, n_local, size=min(n_local, 64))
-    t = time.perf_counter()
-    oracle.attn_rows(qh, kh, vh, probe, w.scale, w.causal)
-    dt = max(time.perf_counter() - t, 1e-6)
-    per_flop = dt / max(row_flops(w, probe), 1.0)
-    rows = probe
-    while True:
-        n = int(min(n_local, max(64, len(rows) * 2)))
-        rows = g.integers(0, n_local, size=n)
-        if row_flops(w, rows) * per_flop >= target_s or n >= n_local:
-            break
-    t = time.perf_counter()
-    oracle.attn_rows(qh, kh, vh, rows, w.scale, w.causal)
-    dt = time.perf_counter() - t
-    return row_flops(w, rows), dt, len(rows), len(heads), oracle.host_threads()
+class OracleSampler:
+    """Times the fp64 oracle on random query rows of a few heads of the
+    workload (the heads are widened to fp64 once)."""
+
+    def __init__(self, w: fin.Workload, x: fin.Inputs, seed: int):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.w = w
+        self.g = np.random.Generator(np.random.PCG64(seed))
+        BH = w.B * w.H
+        self.heads = np.unique(self.g.integers(0, BH, size=min(BH, 4)))
+        self.q = fin.bf16_to_f64(x.q.reshape(BH, w.N, w.d)[self.heads])[None]
+        self.k = fin.bf16_to_f64(x.k.reshape(BH, w.N, w.d)[self.heads])[None]
+        self.v = fin.bf16_to_f64(x.v.reshape(BH, w.N, w.d)[self.heads])[None]
+        self.n_local = len(self.heads) * w.N
+        self.sec_per_flop = None
+
+    def run(self, target_s: float):
+        """One timed sample sized to take about target_s seconds.
+        Returns (flops, seconds, rows)."""
+        w = self.w
+        if self.sec_per_flop is None:
+            probe = self.g.integers(0, self.n_local, size=min(self.n_local, 32))
+            t = time.perf_counter()
+            self.oracle.attn_rows(self.q, self.k, self.v, probe, w.scale, w.causal)
+            self.sec_per_flop = max(time.perf_counter() - t, 1e-6) / max(row_flops(w, probe), 1.0)
+        avg_row = 4.0 * w.d * (w.N + 1) / 2 if w.causal else 4.0 * w.d * w.N
+        n = int(min(self.n_local, max(16, target_s / (self.sec_per_flop * avg_row))))
+        rows = self.g.integers(0, self.n_local, size=n)
+        t = time.perf_counter()
+        self.oracle.attn_rows(self.q, self.k, self.v, rows, w.scale, w.causal)
+        dt = time.perf_counter() - t
+        return row_flops(w, rows), dt, n
+
+    def describe(self, n_rows: int, seconds: float) -> str:
+        return (f"{n_rows} random query rows from {len(self.heads)} heads of the {self.w.name} workload "
+                f"({seconds:.2f} s of fp64 CPU work); host CPU {cpu_model()}")
 
 
 # ------------------------------------------------------------------ reference arm
@@ -217,18 +227,23 @@ def run_reference(args, w: fin.Workload):
     if rank != 0:
         return 0
     x = fin.make_inputs(w)
-    per_step_s = max(0.5, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    # the whole run (warm-up + timed steps) stays near two minutes of CPU work
+    per_step_s = max(0.005, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    sampler = OracleSampler(w, x, seed=w.seed + 17)
     flops_total = 0.0
     secs_total = 0.0
-    rows_n = heads_n = threads = 0
+    rows_total = 0
     for i in range(args.warmup + args.steps):
-        f, s, rows_n, heads_n, threads = oracle_sample(w, x, per_step_s, seed=w.seed + 17 * i)
+        f, s_, n = sampler.run(per_step_s)
         if i >= args.warmup:
             flops_total += f
-            secs_total += s
+            secs_total += s_
+            rows_total += n
     value = flops_total / secs_total / 1e12
-    sample = (f"{rows_n} random query rows per step from {heads_n} heads of the {w.name} workload "
-              f"(~{per_step_s:.1f} s of fp64 CPU work per step); host CPU {cpu_model()}")
+    threads = sampler.oracle.host_threads()
+    sample = (f"per step about {rows_total / args.steps:.0f} random query rows from "
+              f"{len(sampler.heads)} heads of the {w.name} workload (~{per_step_s:.3f} s of fp64 CPU work "
+              f"per step); host CPU {cpu_model()}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -392,10 +407,10 @@ def run_ours(args, w: fin.Workload):
         return 0
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        f, s, n_rows, n_heads, threads = oracle_sample(w, x, args.cpu_seconds, seed=w.seed + 5)
-        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": (f"{n_rows} random query rows from {n_heads} heads of the {w.name} workload, "
-                          f"{s:.1f} s of fp64 CPU work; host CPU {cpu_model()}")}
+        sampler = OracleSampler(w, x, seed=w.seed + 5)
+        f, sec, n_rows = sampler.run(args.cpu_seconds)
+        cpu = {"value": f / sec / 1e12, "unit": "TFLOP/s", "cores": sampler.oracle.host_threads(),
+               "kind": "oracle", "sample": sampler.describe(n_rows, sec)}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_total_ms / args.steps, "higher_is_better": True,
@@ -423,16 +438,22 @@ def run_ours(args, w: fin.Workload):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(fin.WORKLOADS), default="llm_prefill")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,d,causal: a custom shape with N(0,1) values instead of a named workload "
+                         "(for profiling small cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     w = fin.WORKLOADS[args.workload]
+    if args.shape:
+        B, H, N, d, causal = (int(x) for x in args.shape.split(","))
+        w = fin.custom(B, H, N, d, bool(causal), seed=fin.SEED_BASE + 99)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
