@@ -41,21 +41,26 @@ struct FwdParams {
 // no kernel has given up on a wait since the host last cleared it.
 __device__ unsigned int g_status;
 
-// Slow path of a bounded wait: polls the barrier, and every few probes checks
-// the CTA's abort flag, the device status word (another CTA gave up) and the
-// elapsed time. On giving up it records `site` and raises the CTA abort flag.
+// Slow path of a bounded wait. The polling loop touches only the barrier and
+// the clock, so a wait that ends normally costs no memory traffic: the abort
+// flag (shared memory) and the device status word (global memory: another CTA
+// gave up) are read only once the wait has already lasted kQuietNs. On giving
+// up it records `site` and raises the CTA abort flag.
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* cta_abort,
-                                       unsigned site, unsigned long long limit_ns) {
+                                          unsigned site, unsigned long long limit_ns) {
+    constexpr unsigned long long kQuietNs = 100000;  // 100 us
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0) {
+        if ((it & 63u) == 0) {
+            const uint64_t waited = ptx::globaltimer_ns() - t0;
+            if (waited < kQuietNs) continue;
             if (*cta_abort) return false;
             if (*reinterpret_cast<volatile unsigned*>(&g_status) != 0u) {
                 *cta_abort = 1;
                 return false;
             }
-            if (ptx::globaltimer_ns() - t0 > limit_ns) {
+            if (waited > limit_ns) {
                 atomicOr(&g_status, site);
                 *cta_abort = 1;
                 return false;
