@@ -1,5 +1,6 @@
 // C ABI of libfa.so: argument checks, TMA tensor maps, kernel selection and
 // launch. Declarations and the contract of every entry point are in fa.h.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -23,12 +24,41 @@ std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
 
+// Work-queue slots of the persistent kernel: {next unit, CTAs finished},
+// one 128-byte line each. A launch takes the next slot of the ring, finds it
+// zero and leaves it zero; 64 slots let that many launches be in flight on
+// different streams without sharing one.
+constexpr int kSchedSlots = 64;
+constexpr int kSchedSlotWords = 32;
+
 struct DeviceState {
     bool probed = false;
     int status = FA_OK;  // FA_OK, FA_ERR_UNSUPPORTED_ARCH
     int sm_count = 0;
+    unsigned* sched = nullptr;  // kSchedSlots x kSchedSlotWords, allocated on first use
+    std::atomic<unsigned> sched_next{0};
 };
 DeviceState g_devices[kMaxDevices];
+
+// Allocates and zeroes the device's work-queue ring once (the only device
+// allocation the library makes; it lives until the process exits).
+int ensure_sched(DeviceState& st) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (st.sched) return FA_OK;
+    void* ptr = nullptr;
+    const size_t bytes = sizeof(unsigned) * kSchedSlots * kSchedSlotWords;
+    if (cudaMalloc(&ptr, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_LAUNCH;
+    }
+    if (cudaMemset(ptr, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(ptr);
+        return FA_ERR_LAUNCH;
+    }
+    st.sched = static_cast<unsigned*>(ptr);
+    return FA_OK;
+}
 
 int resolve_encode() {
     if (g_encode) return FA_OK;
@@ -240,6 +270,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         std::lock_guard<std::mutex> lock(g_mu);
         prm.wait_limit_ns = g_wait_limit_ns;
     }
+    if (ensure_sched(*st) != FA_OK) return FA_ERR_LAUNCH;
+    prm.sched = st->sched + (st->sched_next.fetch_add(1) % kSchedSlots) * kSchedSlotWords;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int sms = st->sm_count;
     if (d == 64)

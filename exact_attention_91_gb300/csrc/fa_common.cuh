@@ -35,6 +35,7 @@ struct FwdParams {
     int num_q_tiles;      // ceil(N / 128)
     float scale_log2;     // scale * log2(e): scores are kept in base-2 units
     unsigned long long wait_limit_ns;  // give up on an mbarrier wait after this long
+    unsigned* sched;      // work-queue slot {next unit, CTAs finished}; zero at launch, zero again at exit
 };
 
 // Device-wide status word (one per device that loads the library). Zero means

@@ -59,10 +59,14 @@ struct WsCfg {
     static constexpr int kOffRing = kOffQ + 2 * kTileBytes;
     static constexpr int kOffStage = kOffRing + kStages * kTileBytes;  // O staging, one box per tile
     static constexpr int kOffBar = kOffStage + 2 * kBoxBytes;
+    static constexpr int kUnitSlots = 4;                     // work units handed from the TMA thread to the others
     // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] fin
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
+    //           u_full[U] u_empty[U]
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 * kUnitSlots;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit queue
+    static constexpr int kSmemBytes = kOffMisc + 8 + 4 * kUnitSlots + 1024;  // + base alignment slack
+    // arrivals that free a unit-queue slot: the MMA thread and the 8 softmax warps
+    static constexpr uint32_t kUnitConsumers = 9;
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + (D == 128 ? 128 : 64);
     // CTA-wide rendezvous of all 12 warps (setup and teardown)
@@ -91,6 +95,11 @@ struct WsSmem {
     __device__ __forceinline__ uint32_t p_full(int t) const { return bar(6 + 2 * S + t); }
     __device__ __forceinline__ uint32_t o_full(int t) const { return bar(8 + 2 * S + t); }
     __device__ __forceinline__ uint32_t fin() const { return bar(10 + 2 * S); }
+    __device__ __forceinline__ uint32_t u_full(int i) const { return bar(11 + 2 * S + i); }
+    __device__ __forceinline__ uint32_t u_empty(int i) const { return bar(11 + 2 * S + Cfg::kUnitSlots + i); }
+    __device__ __forceinline__ volatile int* unit_slot(int i) const {
+        return reinterpret_cast<volatile int*>(base + Cfg::kOffMisc + 8) + i;
+    }
     __device__ __forceinline__ uint32_t* tmem_slot() const {
         return reinterpret_cast<uint32_t*>(base + Cfg::kOffMisc);
     }
@@ -103,9 +112,11 @@ struct WsSmem {
     }
 };
 
-// Unit u -> (head, 256-row query block). Heads are taken in groups of 16 so
-// that the CTAs running at any moment share few heads and their K/V tiles
-// stay in L2; inside a group the blocks with the most key tiles come first.
+// Unit u -> (head, 256-row query block). CTAs claim units in increasing u from
+// a global counter as they free up. Heads are taken in groups of 16 so that
+// the units in flight at any moment share few heads and their K/V tiles stay
+// in L2; inside a group the blocks with the most key tiles come first, so the
+// lightest units fill the tail.
 __device__ __forceinline__ void unit_coords(int u, int nqb, int BH, int& bh, int& qb) {
     constexpr int kGroup = 16;
     const int per_group = kGroup * nqb;
@@ -119,6 +130,25 @@ __device__ __forceinline__ void unit_coords(int u, int nqb, int BH, int& bh, int
 template <bool CAUSAL>
 __device__ __forceinline__ int kv_tiles_for(int q_tile, int n_k_tiles) {
     return CAUSAL ? min(q_tile + 1, n_k_tiles) : n_k_tiles;
+}
+
+// Next unit of this CTA from the unit queue (consumer side): waits for queue
+// slot `it`, reads it, and frees the slot. `mask` names the calling lanes of
+// the warp (all 32 for a softmax warp, lane 0 alone for the MMA thread); the
+// lowest of them arrives once after all have read. Returns -1 when the CTA has
+// no more work, and -2 if the wait gave up.
+template <int D>
+__device__ __forceinline__ int next_unit(const WsSmem<D>& sm, int it, int lane, unsigned mask,
+                                         const FwdParams& p) {
+    constexpr int U = WsCfg<D>::kUnitSlots;
+    const int slot = it % U;
+    bool ok = wait_phase(sm.u_full(slot), (it / U) & 1, sm.abort_flag(), kStatusTimeoutOther, p.wait_limit_ns);
+    ok = __all_sync(mask, ok);
+    if (!ok) return -2;
+    const int u = *sm.unit_slot(slot);
+    __syncwarp(mask);
+    if (lane == __ffs(mask) - 1) ptx::mbar_arrive(sm.u_empty(slot));
+    return u;
 }
 
 struct WsGeometry {
@@ -146,10 +176,19 @@ __device__ __forceinline__ void ws_load_role(const CUtensorMap& tm_q, const CUte
     ptx::prefetch_tensormap(&tm_v);
     const uint64_t keep = ptx::policy_evict_last();
     const uint64_t stream_once = ptx::policy_evict_first();
+    constexpr int U = Cfg::kUnitSlots;
     uint32_t kv_cnt = 0;
-    int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < g.n_units && ok; u += gridDim.x, ++it) {
+    for (int it = 0; ok; ++it) {
+        // claim the next unit and hand it to the other roles
+        const int qslot = it % U;
+        ok = wait_phase(sm.u_empty(qslot), ((it / U) & 1) ^ 1, abort_flag, kStatusTimeoutOther, lim);
+        if (!ok) break;
+        int u = static_cast<int>(atomicAdd(p.sched, 1u));
+        if (u >= g.n_units) u = -1;
+        *sm.unit_slot(qslot) = u;
+        ptx::mbar_arrive(sm.u_full(qslot));
+        if (u < 0) break;
         int bh, qb;
         unit_coords(u, g.nqb, g.BH, bh, qb);
         const int n1 = kv_tiles_for<CAUSAL>(2 * qb + 1, g.n_k_tiles);
@@ -214,7 +253,6 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
     };
     uint32_t kv_cnt = 0;
     uint32_t p_cnt0 = 0, p_cnt1 = 0;
-    int it = 0;
     bool ok = true;
     auto wait_p = [&](int t) {
         uint32_t& c = t == 0 ? p_cnt0 : p_cnt1;
@@ -226,7 +264,9 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
         ok = ok && wait_phase(sm.kv_full(cnt % S), (cnt / S) & 1, abort_flag, kStatusTimeoutLoad, lim);
         return ok;
     };
-    for (int u = blockIdx.x; u < g.n_units && ok; u += gridDim.x, ++it) {
+    for (int it = 0; ok; ++it) {
+        const int u = next_unit(sm, it, 0, 1u, p);
+        if (u < 0) break;
         int bh, qb;
         unit_coords(u, g.nqb, g.BH, bh, qb);
         const int n0 = kv_tiles_for<CAUSAL>(2 * qb, g.n_k_tiles);
@@ -326,9 +366,11 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
     const uint32_t stage_s = sm.sbase + Cfg::kOffStage + t * kBoxBytes;
     const float c_log2 = p.scale_log2;
     uint32_t s_cnt = 0;
-    int it = 0;
     bool failed = false;
-    for (int u = blockIdx.x; u < g.n_units; u += gridDim.x, ++it) {
+    for (int it = 0;; ++it) {
+        const int u = next_unit(sm, it, lane, 0xffffffffu, p);
+        if (u == -2) failed = true;
+        if (named_bar_or(1 + t, 128, u < 0)) break;  // the warpgroup agrees on stopping
         int bh, qb;
         unit_coords(u, g.nqb, g.BH, bh, qb);
         const int q_tile = 2 * qb + t;
@@ -368,13 +410,14 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = (c > last) ? -INFINITY : s[c];
                 }
+                // four independent chains of 3-input max (two new elements each)
                 mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-                for (int c = 4; c < 64; c += 4) {
-                    mx0 = fmaxf(mx0, s[c]);
-                    mx1 = fmaxf(mx1, s[c + 1]);
-                    mx2 = fmaxf(mx2, s[c + 2]);
-                    mx3 = fmaxf(mx3, s[c + 3]);
+                for (int c = 4; c < 64; c += 8) {
+                    mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+                    mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+                    mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+                    mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
                 }
                 ptx::tmem_wait_ld(r2);
                 ptx::reg_fence(r3);
@@ -389,13 +432,13 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                 for (int c = 64; c < kBlockN; ++c) s[c] = (c > last) ? -INFINITY : s[c];
             }
 #pragma unroll
-            for (int c = 64; c < kBlockN; c += 4) {
-                mx0 = fmaxf(mx0, s[c]);
-                mx1 = fmaxf(mx1, s[c + 1]);
-                mx2 = fmaxf(mx2, s[c + 2]);
-                mx3 = fmaxf(mx3, s[c + 3]);
+            for (int c = 64; c < kBlockN; c += 8) {
+                mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+                mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+                mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+                mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
             }
-            const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_log2;
+            const float m_tile = fmaxf(ptx::fmax3(mx0, mx1, mx2), mx3) * c_log2;
             const bool move = m_tile > m_ref + kTau;
             float alpha = 1.f;
             if (move) {
@@ -415,29 +458,30 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                 }
             }
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;  // fully masked row stays finite
-            float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+            const float2 cc = make_float2(c_log2, c_log2), mm = make_float2(-m_use, -m_use);
+            float2 sum01 = make_float2(0.f, 0.f), sum23 = make_float2(0.f, 0.f);
             // p = 2^(S·c - m) and P (bf16 pairs) over the first 64 columns of S_t,
-            // one 32-column store per 64 keys as soon as they are done
+            // one 32-column store per 64 keys as soon as they are done. The
+            // exponent arguments and the running sums use packed fp32 pairs.
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     const int c = h * 64 + 2 * i;
-                    const float p0 = ptx::ex2_approx(fmaf(s[c], c_log2, -m_use));
-                    const float p1 = ptx::ex2_approx(fmaf(s[c + 1], c_log2, -m_use));
-                    const float p2 = ptx::ex2_approx(fmaf(s[c + 2], c_log2, -m_use));
-                    const float p3 = ptx::ex2_approx(fmaf(s[c + 3], c_log2, -m_use));
-                    sum0 += p0;
-                    sum1 += p1;
-                    sum2 += p2;
-                    sum3 += p3;
-                    r[i] = ptx::pack_bf16x2(p0, p1);
-                    r[i + 1] = ptx::pack_bf16x2(p2, p3);
+                    const float2 x01 = ptx::ffma2(make_float2(s[c], s[c + 1]), cc, mm);
+                    const float2 x23 = ptx::ffma2(make_float2(s[c + 2], s[c + 3]), cc, mm);
+                    const float2 p01 = make_float2(ptx::ex2_approx(x01.x), ptx::ex2_approx(x01.y));
+                    const float2 p23 = make_float2(ptx::ex2_approx(x23.x), ptx::ex2_approx(x23.y));
+                    sum01 = ptx::fadd2(sum01, p01);
+                    sum23 = ptx::fadd2(sum23, p23);
+                    r[i] = ptx::pack_bf16x2(p01.x, p01.y);
+                    r[i + 1] = ptx::pack_bf16x2(p23.x, p23.y);
                 }
                 ptx::tmem_st_32x32b_x32(tS + h * 32, r);
             }
-            l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
+            const float2 sum = ptx::fadd2(sum01, sum23);
+            l = l * alpha + (sum.x + sum.y);
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
             __syncwarp();
@@ -507,8 +551,12 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (warp == 9 && lane == 0) {
             for (int i = 0; i < Cfg::kNumBars; ++i) {
-                const bool p_full = sm.bar(i) == sm.p_full(0) || sm.bar(i) == sm.p_full(1);
-                ptx::mbar_init(sm.bar(i), p_full ? 4 : 1);  // P: one arrival per softmax warp
+                const uint32_t b = sm.bar(i);
+                uint32_t count = 1;
+                if (b == sm.p_full(0) || b == sm.p_full(1)) count = 4;  // one arrival per softmax warp
+                for (int q = 0; q < Cfg::kUnitSlots; ++q)
+                    if (b == sm.u_empty(q)) count = Cfg::kUnitConsumers;
+                ptx::mbar_init(b, count);
             }
             *sm.abort_flag() = 0;
             ptx::fence_mbar_init();
@@ -525,6 +573,16 @@ __global__ void __launch_bounds__(384, 1)
         }
         ptx::tc_fence_before_sync();
         ptx::named_bar_sync(Cfg::kBarAll, Cfg::kThreads);
+        if (warp == 9 && lane == 0) {
+            // every CTA has claimed its last unit before it counts itself done,
+            // so the last one can put the queue slot back to zero for the next launch
+            __threadfence();
+            if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+                p.sched[0] = 0u;
+                p.sched[1] = 0u;
+                __threadfence();
+            }
+        }
         if (warp == 8) {
             if (lane == 0) {
                 ptx::mma_commit(sm.fin());

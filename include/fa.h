@@ -20,7 +20,7 @@
  *
  * Plain C types only: device pointers are `const void*` / `void*`, the CUDA
  * stream is passed as `void*` (a cudaStream_t; NULL is the legacy default
- * stream). No function allocates device memory.
+ * stream).
  */
 #ifndef FA_H_
 #define FA_H_
@@ -62,7 +62,13 @@ typedef enum fa_status {
  * stream   cudaStream_t to run on, as void*; NULL = legacy default stream.
  *
  * Ownership: the caller allocates and owns every buffer; the library keeps
- * no pointer after the call returns. The call is asynchronous: argument errors
+ * no pointer after the call returns. The library's own state is one 8 KB
+ * device buffer per device (work-queue counters for the persistent kernel),
+ * allocated and zeroed by the first fa_fwd call on that device (that first
+ * call synchronises the device) and kept until the process exits. Each
+ * launch uses one of its 64 counter slots in turn and leaves it zeroed, so up
+ * to 64 launches may be in flight at once on different streams. The call is
+ * asynchronous: argument errors
  * are returned before anything is queued; faults inside the kernel appear at
  * the caller's next synchronisation, and a kernel that gave up on a wait
  * leaves its O/LSE rows unwritten and reports through fa_device_status().
