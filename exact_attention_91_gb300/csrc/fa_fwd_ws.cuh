@@ -61,14 +61,21 @@ struct WsCfg {
     static constexpr int kOffBar = kOffStage + 2 * kBoxBytes;
     static constexpr int kUnitSlots = 4;                     // work units handed from the TMA thread to the others
     // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] fin
-    //           u_full[U] u_empty[U]
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 * kUnitSlots;
+    //           u_full[U] u_empty[U] pv_done[2]
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 * kUnitSlots + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit queue
     static constexpr int kSmemBytes = kOffMisc + 8 + 4 * kUnitSlots + 1024;  // + base alignment slack
     // arrivals that free a unit-queue slot: the MMA thread and the 8 softmax warps
     static constexpr uint32_t kUnitConsumers = 9;
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + (D == 128 ? 128 : 64);
+    // P (bf16 pairs, 64 columns per tile). With d = 64 it has columns of its
+    // own; with d = 128 all 512 columns are taken and P overwrites the first
+    // 64 columns of S_t. An MMA that writes S_t may then start only after the
+    // P·V that reads P_t from those columns has completed: tcgen05.mma keeps
+    // issue order only between MMAs into the same accumulator.
+    static constexpr bool kPOverS = D == 128;
+    static constexpr uint32_t kTmemP0 = kPOverS ? kTmemS0 : 384, kTmemP1 = kPOverS ? kTmemS1 : 448;
     // CTA-wide rendezvous of all 12 warps (setup and teardown)
     static constexpr uint32_t kBarAll = 15;
 };
@@ -97,6 +104,7 @@ struct WsSmem {
     __device__ __forceinline__ uint32_t fin() const { return bar(10 + 2 * S); }
     __device__ __forceinline__ uint32_t u_full(int i) const { return bar(11 + 2 * S + i); }
     __device__ __forceinline__ uint32_t u_empty(int i) const { return bar(11 + 2 * S + Cfg::kUnitSlots + i); }
+    __device__ __forceinline__ uint32_t pv_done(int t) const { return bar(11 + 2 * S + 2 * Cfg::kUnitSlots + t); }
     __device__ __forceinline__ volatile int* unit_slot(int i) const {
         return reinterpret_cast<volatile int*>(base + Cfg::kOffMisc + 8) + i;
     }
@@ -241,19 +249,44 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
     };
     // O_t += P_t·V over 128 keys in steps of 16 (2048 bytes of V each);
     // V is MN-major: 64-wide swizzle atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
-    auto issue_pv = [&](int t, uint32_t sV, bool accumulate) {
+    auto issue_pv_mma = [&](int t, uint32_t sV, bool accumulate) {
         const uint64_t b0 = ptx::sdesc_sw128(sV, kBoxBytes, 1024);
-        const uint32_t tS = tmem + (t == 0 ? Cfg::kTmemS0 : Cfg::kTmemS1);
+        const uint32_t tP = tmem + (t == 0 ? Cfg::kTmemP0 : Cfg::kTmemP1);
         const uint32_t tO = tmem + (t == 0 ? Cfg::kTmemO0 : Cfg::kTmemO1);
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            ptx::mma_ts(tO, tS + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
+            ptx::mma_ts(tO, tP + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
                         (accumulate || kk > 0) ? 1u : 0u);
         }
     };
     uint32_t kv_cnt = 0;
     uint32_t p_cnt0 = 0, p_cnt1 = 0;
+    uint32_t pv_cnt0 = 0, pv_cnt1 = 0;  // P·V MMAs of each tile whose completion has not been awaited
+    uint32_t pv_seen0 = 0, pv_seen1 = 0;
     bool ok = true;
+    // P·V of tile t; when P overlays S_t its completion is tracked so the next S_t can wait for it
+    auto issue_pv = [&](int t, uint32_t sV, bool accumulate) {
+        issue_pv_mma(t, sV, accumulate);
+        if (Cfg::kPOverS) {
+            ptx::mma_commit(sm.pv_done(t));
+            ++(t == 0 ? pv_cnt0 : pv_cnt1);
+        }
+    };
+    // S_t = Q_t·K^T, after the last P·V that read P_t out of S_t's columns has completed
+    auto issue_s_safe = [&](int t, uint32_t sK) {
+        if (Cfg::kPOverS) {
+            uint32_t& seen = t == 0 ? pv_seen0 : pv_seen1;
+            const uint32_t issued = t == 0 ? pv_cnt0 : pv_cnt1;
+            while (ok && seen < issued) {
+                ok = wait_phase(sm.pv_done(t), seen & 1, abort_flag, kStatusTimeoutMma, lim);
+                ++seen;
+            }
+            if (!ok) return false;
+            ptx::tc_fence_after_sync();
+        }
+        issue_s(t, sK);
+        return true;
+    };
     auto wait_p = [&](int t) {
         uint32_t& c = t == 0 ? p_cnt0 : p_cnt1;
         ok = ok && wait_phase(sm.p_full(t), c & 1, abort_flag, kStatusTimeoutSoftmax, lim);
@@ -275,12 +308,12 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
         // first key tile: S_0 and S_1
         if (!(wait_phase(sm.q_full(0), it & 1, abort_flag, kStatusTimeoutLoad, lim) && wait_kv(k0))) break;
         ptx::tc_fence_after_sync();
-        issue_s(0, sm.ring(k0));
+        if (!issue_s_safe(0, sm.ring(k0))) break;
         ptx::mma_commit(sm.s_full(0));
         if (n0 == 1) ptx::mma_commit(sm.q_empty(0));
         if (!wait_phase(sm.q_full(1), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
         ptx::tc_fence_after_sync();
-        issue_s(1, sm.ring(k0));
+        if (!issue_s_safe(1, sm.ring(k0))) break;
         ptx::mma_commit(sm.s_full(1));
         if (n1 == 1) ptx::mma_commit(sm.q_empty(1));
         ptx::mma_commit(sm.kv_empty(k0 % S));
@@ -296,7 +329,7 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
                 if (j < n0) {
                     if (!wait_kv(kj)) break;
                     ptx::tc_fence_after_sync();
-                    issue_s(0, sm.ring(kj));
+                    if (!issue_s_safe(0, sm.ring(kj))) break;
                     ptx::mma_commit(sm.s_full(0));
                     if (j == n0 - 1) ptx::mma_commit(sm.q_empty(0));
                 } else {
@@ -309,7 +342,7 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
             ptx::mma_commit(sm.kv_empty(vprev % S));
             if (!wait_kv(kj)) break;
             ptx::tc_fence_after_sync();
-            issue_s(1, sm.ring(kj));
+            if (!issue_s_safe(1, sm.ring(kj))) break;
             ptx::mma_commit(sm.s_full(1));
             if (j == n1 - 1) ptx::mma_commit(sm.q_empty(1));
             ptx::mma_commit(sm.kv_empty(kj % S));
@@ -362,6 +395,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + (t == 0 ? Cfg::kTmemS0 : Cfg::kTmemS1) + lane_base;
     const uint32_t tO = tmem + (t == 0 ? Cfg::kTmemO0 : Cfg::kTmemO1) + lane_base;
+    const uint32_t tP = tmem + (t == 0 ? Cfg::kTmemP0 : Cfg::kTmemP1) + lane_base;
     uint8_t* stage = sm.base + Cfg::kOffStage + t * kBoxBytes;
     const uint32_t stage_s = sm.sbase + Cfg::kOffStage + t * kBoxBytes;
     const float c_log2 = p.scale_log2;
@@ -460,7 +494,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;  // fully masked row stays finite
             const float2 cc = make_float2(c_log2, c_log2), mm = make_float2(-m_use, -m_use);
             float2 sum01 = make_float2(0.f, 0.f), sum23 = make_float2(0.f, 0.f);
-            // p = 2^(S·c - m) and P (bf16 pairs) over the first 64 columns of S_t,
+            // p = 2^(S·c - m) and P (bf16 pairs, 64 columns at tP),
             // one 32-column store per 64 keys as soon as they are done. The
             // exponent arguments and the running sums use packed fp32 pairs.
 #pragma unroll
@@ -478,7 +512,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                     r[i] = ptx::pack_bf16x2(p01.x, p01.y);
                     r[i + 1] = ptx::pack_bf16x2(p23.x, p23.y);
                 }
-                ptx::tmem_st_32x32b_x32(tS + h * 32, r);
+                ptx::tmem_st_32x32b_x32(tP + h * 32, r);
             }
             const float2 sum = ptx::fadd2(sum01, sum23);
             l = l * alpha + (sum.x + sum.y);
