@@ -61,8 +61,8 @@ struct WsCfg {
     static constexpr int kOffBar = kOffStage + 2 * kBoxBytes;
     static constexpr int kUnitSlots = 4;                     // work units handed from the TMA thread to the others
     // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] fin
-    //           u_full[U] u_empty[U] pv_done[2]
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 * kUnitSlots + 2;
+    //           u_full[U] u_empty[U] pv_done[2] s_free[2]
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 * kUnitSlots + 2 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit queue
     static constexpr int kSmemBytes = kOffMisc + 8 + 4 * kUnitSlots + 1024;  // + base alignment slack
     // arrivals that free a unit-queue slot: the MMA thread and the 8 softmax warps
@@ -75,6 +75,10 @@ struct WsCfg {
     // P·V that reads P_t from those columns has completed: tcgen05.mma keeps
     // issue order only between MMAs into the same accumulator.
     static constexpr bool kPOverS = D == 128;
+    // With P in columns of its own, S_t(j+1) may be computed as soon as the
+    // softmax has read S_t(j) into registers (an "S consumed" barrier); the
+    // softmax then waits for P·V(j) only before it writes P or rescales O.
+    static constexpr bool kEarlyS = !kPOverS;
     static constexpr uint32_t kTmemP0 = kPOverS ? kTmemS0 : 384, kTmemP1 = kPOverS ? kTmemS1 : 448;
     // CTA-wide rendezvous of all 12 warps (setup and teardown)
     static constexpr uint32_t kBarAll = 15;
@@ -105,6 +109,7 @@ struct WsSmem {
     __device__ __forceinline__ uint32_t u_full(int i) const { return bar(11 + 2 * S + i); }
     __device__ __forceinline__ uint32_t u_empty(int i) const { return bar(11 + 2 * S + Cfg::kUnitSlots + i); }
     __device__ __forceinline__ uint32_t pv_done(int t) const { return bar(11 + 2 * S + 2 * Cfg::kUnitSlots + t); }
+    __device__ __forceinline__ uint32_t s_free(int t) const { return bar(13 + 2 * S + 2 * Cfg::kUnitSlots + t); }
     __device__ __forceinline__ volatile int* unit_slot(int i) const {
         return reinterpret_cast<volatile int*>(base + Cfg::kOffMisc + 8) + i;
     }
@@ -261,18 +266,18 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
     };
     uint32_t kv_cnt = 0;
     uint32_t p_cnt0 = 0, p_cnt1 = 0;
-    uint32_t pv_cnt0 = 0, pv_cnt1 = 0;  // P·V MMAs of each tile whose completion has not been awaited
-    uint32_t pv_seen0 = 0, pv_seen1 = 0;
+    uint32_t pv_cnt0 = 0, pv_cnt1 = 0, pv_seen0 = 0, pv_seen1 = 0;  // P·V MMAs issued / seen completed
+    uint32_t s_cnt0 = 0, s_cnt1 = 0, sf_seen0 = 0, sf_seen1 = 0;    // S MMAs issued / seen consumed
     bool ok = true;
-    // P·V of tile t; when P overlays S_t its completion is tracked so the next S_t can wait for it
+    // P·V of tile t; its completion is published on pv_done(t)
     auto issue_pv = [&](int t, uint32_t sV, bool accumulate) {
         issue_pv_mma(t, sV, accumulate);
-        if (Cfg::kPOverS) {
-            ptx::mma_commit(sm.pv_done(t));
-            ++(t == 0 ? pv_cnt0 : pv_cnt1);
-        }
+        ptx::mma_commit(sm.pv_done(t));
+        ++(t == 0 ? pv_cnt0 : pv_cnt1);
     };
-    // S_t = Q_t·K^T, after the last P·V that read P_t out of S_t's columns has completed
+    // S_t = Q_t·K^T once S_t's columns are free: when P overlays S_t, after
+    // the last P·V that read P_t has completed; otherwise after the softmax
+    // has read every earlier S_t.
     auto issue_s_safe = [&](int t, uint32_t sK) {
         if (Cfg::kPOverS) {
             uint32_t& seen = t == 0 ? pv_seen0 : pv_seen1;
@@ -281,10 +286,18 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
                 ok = wait_phase(sm.pv_done(t), seen & 1, abort_flag, kStatusTimeoutMma, lim);
                 ++seen;
             }
-            if (!ok) return false;
-            ptx::tc_fence_after_sync();
+        } else {
+            uint32_t& seen = t == 0 ? sf_seen0 : sf_seen1;
+            const uint32_t issued = t == 0 ? s_cnt0 : s_cnt1;
+            while (ok && seen < issued) {
+                ok = wait_phase(sm.s_free(t), seen & 1, abort_flag, kStatusTimeoutSoftmax, lim);
+                ++seen;
+            }
         }
+        if (!ok) return false;
+        ptx::tc_fence_after_sync();
         issue_s(t, sK);
+        ++(t == 0 ? s_cnt0 : s_cnt1);
         return true;
     };
     auto wait_p = [&](int t) {
@@ -319,6 +332,31 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
         ptx::mma_commit(sm.kv_empty(k0 % S));
         for (int j = 1; j < n1; ++j) {
             const uint32_t kj = k0 + 2 * j, vprev = k0 + 2 * j - 1;
+            if (Cfg::kEarlyS) {
+                // S_t(j) first: it only needs K_j and the softmax's read of S_t(j-1)
+                if (!wait_kv(kj)) break;
+                if (j < n0) {
+                    if (!issue_s_safe(0, sm.ring(kj))) break;
+                    ptx::mma_commit(sm.s_full(0));
+                    if (j == n0 - 1) ptx::mma_commit(sm.q_empty(0));
+                }
+                if (!issue_s_safe(1, sm.ring(kj))) break;
+                ptx::mma_commit(sm.s_full(1));
+                if (j == n1 - 1) ptx::mma_commit(sm.q_empty(1));
+                ptx::mma_commit(sm.kv_empty(kj % S));
+                if (!wait_kv(vprev)) break;
+                if (j <= n0) {
+                    if (!wait_p(0)) break;
+                    ptx::tc_fence_after_sync();
+                    issue_pv(0, sm.ring(vprev), j > 1);
+                    if (j == n0) ptx::mma_commit(sm.o_full(0));
+                }
+                if (!wait_p(1)) break;
+                ptx::tc_fence_after_sync();
+                issue_pv(1, sm.ring(vprev), j > 1);
+                ptx::mma_commit(sm.kv_empty(vprev % S));
+                continue;
+            }
             // P·V needs only V_{j-1}; K_j may still be in flight. (A second
             // wait on K_j's slot is immediate: it is not refilled before release.)
             if (!wait_kv(vprev)) break;
@@ -328,7 +366,6 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
                 issue_pv(0, sm.ring(vprev), j > 1);
                 if (j < n0) {
                     if (!wait_kv(kj)) break;
-                    ptx::tc_fence_after_sync();
                     if (!issue_s_safe(0, sm.ring(kj))) break;
                     ptx::mma_commit(sm.s_full(0));
                     if (j == n0 - 1) ptx::mma_commit(sm.q_empty(0));
@@ -341,7 +378,6 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
             issue_pv(1, sm.ring(vprev), j > 1);
             ptx::mma_commit(sm.kv_empty(vprev % S));
             if (!wait_kv(kj)) break;
-            ptx::tc_fence_after_sync();
             if (!issue_s_safe(1, sm.ring(kj))) break;
             ptx::mma_commit(sm.s_full(1));
             if (j == n1 - 1) ptx::mma_commit(sm.q_empty(1));
@@ -400,6 +436,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
     const uint32_t stage_s = sm.sbase + Cfg::kOffStage + t * kBoxBytes;
     const float c_log2 = p.scale_log2;
     uint32_t s_cnt = 0;
+    uint32_t p_made = 0, pv_seen = 0;  // P tiles written / P·V completions observed (early-S mode)
     bool failed = false;
     for (int it = 0;; ++it) {
         const int u = next_unit(sm, it, lane, 0xffffffffu, p);
@@ -444,10 +481,11 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = (c > last) ? -INFINITY : s[c];
                 }
-                // four independent chains of 3-input max (two new elements each)
-                mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                // four independent chains of 3-input max (two new elements each),
+                // over columns 0-63 only: 64-127 are still being loaded
+                mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-                for (int c = 4; c < 64; c += 8) {
+                for (int c = 8; c < 64; c += 8) {
                     mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
                     mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
                     mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
@@ -460,6 +498,12 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                     s[64 + i] = __uint_as_float(r2[i]);
                     s[96 + i] = __uint_as_float(r3[i]);
                 }
+            }
+            if (Cfg::kEarlyS) {
+                // S_t is in registers: the MMA warp may overwrite it with the next tile
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(sm.s_free(t));
             }
             if (need_mask) {
 #pragma unroll
@@ -479,7 +523,21 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                 alpha = ptx::ex2_approx(m_ref - m_tile);  // 0 on the first visible tile
                 m_ref = m_tile;
             }
-            // O_t *= alpha; the previous P·V of this tile finished before S_t was committed
+            if (Cfg::kEarlyS) {
+                // the P·V of every earlier P of this tile must be done before P and O are touched
+                bool okp = true;
+                while (okp && pv_seen < p_made) {
+                    okp = wait_phase(sm.pv_done(t), pv_seen & 1, abort_flag, kStatusTimeoutMma, lim);
+                    ++pv_seen;
+                }
+                if (!__all_sync(0xffffffffu, okp)) {
+                    failed = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+            }
+            // O_t *= alpha. (Without early S, the previous P·V of this tile
+            // finished before S_t was committed.)
             if (j > 0 && __any_sync(0xffffffffu, move)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 8; ++c) {
@@ -520,6 +578,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(sm.p_full(t));
+            ++p_made;
         }
         // ---- epilogue of tile t: O_t / l -> bf16 -> staging box -> TMA store; LSE
         bool ok = !failed && wait_phase(sm.o_full(t), it & 1, abort_flag, kStatusTimeoutMma, lim);
@@ -587,7 +646,8 @@ __global__ void __launch_bounds__(384, 1)
             for (int i = 0; i < Cfg::kNumBars; ++i) {
                 const uint32_t b = sm.bar(i);
                 uint32_t count = 1;
-                if (b == sm.p_full(0) || b == sm.p_full(1)) count = 4;  // one arrival per softmax warp
+                if (b == sm.p_full(0) || b == sm.p_full(1) || b == sm.s_free(0) || b == sm.s_free(1))
+                    count = 4;  // one arrival per softmax warp
                 for (int q = 0; q < Cfg::kUnitSlots; ++q)
                     if (b == sm.u_empty(q)) count = Cfg::kUnitConsumers;
                 ptx::mbar_init(b, count);
