@@ -15,11 +15,11 @@ import os
 
 from .build import LIB_PATH
 
-__all__ = ["FaError", "load_library", "fa_fwd", "fa_strerror", "fa_device_status",
+__all__ = ["FaError", "load_library", "fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
            "fa_set_wait_limit_ns", "fa_abi_version", "attention_forward", "EXPORTED_SYMBOLS"]
 
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_strerror", "fa_device_status", "fa_set_wait_limit_ns",
-                    "fa_abi_version")
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
+                    "fa_set_wait_limit_ns", "fa_abi_version")
 
 FA_OK = 0
 FA_ERR_DEVICE_TIMEOUT = -8
@@ -46,6 +46,8 @@ def load_library(path: str | None = None):
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd_noalloc.restype = i
     lib.fa_strerror.argtypes = [i]
     lib.fa_strerror.restype = ctypes.c_char_p
     lib.fa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -64,6 +66,16 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, N: i
     """The C ``fa_fwd``: device pointers as ints, returns the status code."""
     return load_library().fa_fwd(q, k, v, o, lse or None, B, H, N, d, scale, int(bool(causal)),
                                  stream or None)
+
+
+def fa_fwd_noalloc(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, N: int, d: int,
+                   scale: float, causal: bool, stream: int | None) -> int:
+    """The C ``fa_fwd_noalloc``: ``fa_fwd`` for callers that cannot let the
+    library allocate device memory (its scratch is a fixed array inside the
+    library). Calls whose kernels overlap on the GPU share that scratch and
+    must not be issued. Returns the status code."""
+    return load_library().fa_fwd_noalloc(q, k, v, o, lse or None, B, H, N, d, scale, int(bool(causal)),
+                                         stream or None)
 
 
 def fa_strerror(status: int) -> str:

@@ -281,3 +281,107 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// fa_fwd keeps its work-queue counters in device memory that the library
+// allocates with cudaMalloc on the first call. Some callers cannot have any
+// allocation happen inside a library call: code running where cudaMalloc is
+// forbidden or would synchronise the device at the wrong moment (inside a
+// custom allocator or memory-pool callback, under a caller-side memory budget
+// that must account for every byte, or in a runtime that pre-plans all device
+// memory up front). fa_fwd_noalloc runs the same kernel with its scratch in
+// the fixed array below, which every GPU that loads the library holds until
+// the process exits. It never calls cudaMalloc, cudaFree or any allocating
+// routine.
+namespace {
+
+// One work-queue slot {next unit, CTAs finished}, padded to a 128-byte line.
+constexpr int kNoAllocScratchWords = 32;
+static __device__ __align__(256) unsigned g_noalloc_scratch[kNoAllocScratchWords];
+
+// Device address of g_noalloc_scratch, per device. In host code the array's
+// name is only a host-side stand-in, so the kernel must be given this
+// address, looked up once per device with that device current.
+unsigned* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(int dev, unsigned** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return FA_ERR_LAUNCH;
+        }
+        g_noalloc_ptr[dev] = static_cast<unsigned*>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int N, int d, float scale, int causal, void* stream) {
+    if (!q || !k || !v || !o) return FA_ERR_NULL_PTR;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long n_q_tiles = (static_cast<long long>(N) + fa::kBlockM - 1) / fa::kBlockM;
+    if (BH > 0x7fffffffLL || BH * n_q_tiles > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
+    // The scratch is one fixed work-queue slot whatever the shape; what it
+    // limits is the unit counter, which must hold every unit plus one
+    // over-claim per CTA.
+    const long long units = ((static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM)) * BH;
+    if (units + 65536LL > 0xffffffffLL) return FA_ERR_BAD_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEAD_DIM;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_MISALIGNED;
+    const size_t tensor_bytes = static_cast<size_t>(BH) * N * d * 2;
+    const size_t lse_bytes = static_cast<size_t>(BH) * N * 4;
+    if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
+        overlaps(o, tensor_bytes, v, tensor_bytes))
+        return FA_ERR_ALIAS;
+    if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
+                overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, o, tensor_bytes)))
+        return FA_ERR_ALIAS;
+
+    int dev = -1;
+    DeviceState* st = nullptr;
+    int rc = probe_device(&dev, &st);
+    if (rc != FA_OK) return rc;
+    unsigned* scratch = nullptr;
+    if (noalloc_scratch(dev, &scratch) != FA_OK) return FA_ERR_LAUNCH;
+
+    CUtensorMap tq, tk, tv, to;
+    const int bh = static_cast<int>(BH);
+    if (encode_map(&tq, q, bh, N, d) != FA_OK || encode_map(&tk, k, bh, N, d) != FA_OK ||
+        encode_map(&tv, v, bh, N, d) != FA_OK || encode_map(&to, o, bh, N, d) != FA_OK)
+        return FA_ERR_LAUNCH;
+
+    fa::FwdParams prm{};
+    prm.lse = lse;
+    prm.N = N;
+    prm.num_heads_total = bh;
+    prm.num_q_tiles = static_cast<int>(n_q_tiles);
+    prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        prm.wait_limit_ns = g_wait_limit_ns;
+    }
+    prm.sched = scratch;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the two counters must start at zero (the kernel also leaves them zero)
+    if (cudaMemsetAsync(scratch, 0, 2 * sizeof(unsigned), s) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_LAUNCH;
+    }
+    const int sms = st->sm_count;
+    if (d == 64)
+        return causal ? launch_ws<64, true>(tq, tk, tv, to, prm, dev, sms, s)
+                      : launch_ws<64, false>(tq, tk, tv, to, prm, dev, sms, s);
+    return causal ? launch_ws<128, true>(tq, tk, tv, to, prm, dev, sms, s)
+                  : launch_ws<128, false>(tq, tk, tv, to, prm, dev, sms, s);
+}

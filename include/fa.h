@@ -77,6 +77,30 @@ typedef enum fa_status {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, void* stream);
 
+/*
+ * fa_fwd_noalloc — the same attention forward pass as fa_fwd, for callers
+ * that cannot let a library call allocate device memory: code running inside
+ * an allocator or memory-pool callback, under a memory budget that must
+ * account for every byte, or in a runtime that plans all device memory
+ * before it starts. (The pages describe no such entry point; it is part of
+ * this library's interface only.)
+ *
+ * Arguments, layouts, ownership and errors are those of fa_fwd. It never calls
+ * cudaMalloc, cudaFree or any allocating routine: its scratch (one 128-byte
+ * work-queue slot) is a fixed array inside the library that every GPU which
+ * loads the library keeps until the process exits. The first call on a
+ * device looks up that array's device address (with that device current);
+ * make the first call before any stream capture. Each call clears the slot's
+ * counters on `stream` before its kernel, and every call shares the one slot:
+ * calls whose kernels overlap on the GPU (different streams, no ordering
+ * between them) race on it and must not be issued. The scratch does not grow
+ * with the problem; the one size it limits is the unit count
+ * B*H*ceil(N/256), which must stay below 2^32 - 65536 (FA_ERR_BAD_SHAPE
+ * otherwise; fa_fwd's own limits are stricter).
+ */
+int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, float scale, int causal, void* stream);
+
 /* Static English text for a return code (never NULL). */
 const char* fa_strerror(int status);
 
