@@ -68,18 +68,18 @@ struct WsCfg {
     // arrivals that free a unit-queue slot: the MMA thread and the 8 softmax warps
     static constexpr uint32_t kUnitConsumers = 9;
     static constexpr int kTmemCols = 512;
-    static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + (D == 128 ? 128 : 64);
-    // P (bf16 pairs, 64 columns per tile). With d = 64 it has columns of its
-    // own; with d = 128 all 512 columns are taken and P overwrites the first
-    // 64 columns of S_t. An MMA that writes S_t may then start only after the
-    // P·V that reads P_t from those columns has completed: tcgen05.mma keeps
-    // issue order only between MMAs into the same accumulator.
-    static constexpr bool kPOverS = D == 128;
-    // With P in columns of its own, S_t(j+1) may be computed as soon as the
-    // softmax has read S_t(j) into registers (an "S consumed" barrier); the
-    // softmax then waits for P·V(j) only before it writes P or rescales O.
-    static constexpr bool kEarlyS = !kPOverS;
-    static constexpr uint32_t kTmemP0 = kPOverS ? kTmemS0 : 384, kTmemP1 = kPOverS ? kTmemS1 : 448;
+    // TMEM columns. P (bf16 pairs, 64 columns per tile) never overlays S, so
+    // no MMA that writes S can race a P·V that is still reading P: tcgen05.mma
+    // keeps issue order only between MMAs into the same accumulator.
+    //  d = 128: one S buffer shared by the two tiles, used alternately (each
+    //           softmax copies S into registers at once); P0, P1, O0, O1.
+    //  d = 64:  an S buffer per tile, so S_t(j+1) can be computed as soon as
+    //           the softmax has read S_t(j) ("early S"); P0, P1, O0, O1.
+    static constexpr bool kSharedS = D == 128;
+    static constexpr bool kEarlyS = !kSharedS;
+    static constexpr uint32_t kTmemS0 = 0, kTmemS1 = kSharedS ? 0 : 128;
+    static constexpr uint32_t kTmemP0 = kSharedS ? 128 : 384, kTmemP1 = kSharedS ? 192 : 448;
+    static constexpr uint32_t kTmemO0 = 256, kTmemO1 = 256 + D;
     // CTA-wide rendezvous of all 12 warps (setup and teardown)
     static constexpr uint32_t kBarAll = 15;
 };
@@ -266,38 +266,31 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
     };
     uint32_t kv_cnt = 0;
     uint32_t p_cnt0 = 0, p_cnt1 = 0;
-    uint32_t pv_cnt0 = 0, pv_cnt1 = 0, pv_seen0 = 0, pv_seen1 = 0;  // P·V MMAs issued / seen completed
-    uint32_t s_cnt0 = 0, s_cnt1 = 0, sf_seen0 = 0, sf_seen1 = 0;    // S MMAs issued / seen consumed
+    // S MMAs issued / seen consumed by the softmax, per S buffer (one shared buffer with d = 128)
+    uint32_t s_cnt0 = 0, s_cnt1 = 0, sf_seen0 = 0, sf_seen1 = 0;
     bool ok = true;
-    // P·V of tile t; its completion is published on pv_done(t)
+    // P·V of tile t. In early-S mode its completion is published on pv_done(t)
+    // for the softmax, which must not overwrite P_t or O_t before it.
     auto issue_pv = [&](int t, uint32_t sV, bool accumulate) {
+        ptx::tc_fence_after_sync();
         issue_pv_mma(t, sV, accumulate);
-        ptx::mma_commit(sm.pv_done(t));
-        ++(t == 0 ? pv_cnt0 : pv_cnt1);
+        if (Cfg::kEarlyS) ptx::mma_commit(sm.pv_done(t));
     };
-    // S_t = Q_t·K^T once S_t's columns are free: when P overlays S_t, after
-    // the last P·V that read P_t has completed; otherwise after the softmax
-    // has read every earlier S_t.
+    // S_t = Q_t·K^T once its S buffer is free: the softmax has read every
+    // earlier S written there.
     auto issue_s_safe = [&](int t, uint32_t sK) {
-        if (Cfg::kPOverS) {
-            uint32_t& seen = t == 0 ? pv_seen0 : pv_seen1;
-            const uint32_t issued = t == 0 ? pv_cnt0 : pv_cnt1;
-            while (ok && seen < issued) {
-                ok = wait_phase(sm.pv_done(t), seen & 1, abort_flag, kStatusTimeoutMma, lim);
-                ++seen;
-            }
-        } else {
-            uint32_t& seen = t == 0 ? sf_seen0 : sf_seen1;
-            const uint32_t issued = t == 0 ? s_cnt0 : s_cnt1;
-            while (ok && seen < issued) {
-                ok = wait_phase(sm.s_free(t), seen & 1, abort_flag, kStatusTimeoutSoftmax, lim);
-                ++seen;
-            }
+        const int b = Cfg::kSharedS ? 0 : t;
+        uint32_t& seen = b == 0 ? sf_seen0 : sf_seen1;
+        uint32_t& issued = b == 0 ? s_cnt0 : s_cnt1;
+        while (ok && seen < issued) {
+            ok = wait_phase(sm.s_free(b), seen & 1, abort_flag, kStatusTimeoutSoftmax, lim);
+            ++seen;
         }
         if (!ok) return false;
         ptx::tc_fence_after_sync();
         issue_s(t, sK);
-        ++(t == 0 ? s_cnt0 : s_cnt1);
+        ++issued;
+        ptx::mma_commit(sm.s_full(t));
         return true;
     };
     auto wait_p = [&](int t) {
@@ -316,88 +309,80 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
         int bh, qb;
         unit_coords(u, g.nqb, g.BH, bh, qb);
         const int n0 = kv_tiles_for<CAUSAL>(2 * qb, g.n_k_tiles);
-        const int n1 = kv_tiles_for<CAUSAL>(2 * qb + 1, g.n_k_tiles);
-        const uint32_t k0 = kv_cnt;  // ring position of K_0; V_j = K_j + 1, K_j = k0 + 2j
-        // first key tile: S_0 and S_1
-        if (!(wait_phase(sm.q_full(0), it & 1, abort_flag, kStatusTimeoutLoad, lim) && wait_kv(k0))) break;
-        ptx::tc_fence_after_sync();
-        if (!issue_s_safe(0, sm.ring(k0))) break;
-        ptx::mma_commit(sm.s_full(0));
-        if (n0 == 1) ptx::mma_commit(sm.q_empty(0));
+        const int n1 = kv_tiles_for<CAUSAL>(2 * qb + 1, g.n_k_tiles);  // n0 <= n1 <= n0 + 1
+        const uint32_t k0 = kv_cnt;  // ring position of K_0; K_j = k0 + 2j, V_j = K_j + 1
+        auto K = [&](int j) { return k0 + 2u * j; };
+        auto V = [&](int j) { return k0 + 2u * j + 1u; };
+        if (!wait_phase(sm.q_full(0), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
         if (!wait_phase(sm.q_full(1), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
-        ptx::tc_fence_after_sync();
-        if (!issue_s_safe(1, sm.ring(k0))) break;
-        ptx::mma_commit(sm.s_full(1));
-        if (n1 == 1) ptx::mma_commit(sm.q_empty(1));
-        ptx::mma_commit(sm.kv_empty(k0 % S));
-        for (int j = 1; j < n1; ++j) {
-            const uint32_t kj = k0 + 2 * j, vprev = k0 + 2 * j - 1;
-            if (Cfg::kEarlyS) {
-                // S_t(j) first: it only needs K_j and the softmax's read of S_t(j-1)
-                if (!wait_kv(kj)) break;
+        if (Cfg::kSharedS) {
+            // TC order per key tile j: S0(j), PV1(j-1), S1(j), PV0(j). Each P·V
+            // of a tile precedes that tile's next S, so the commit of S_t(j)
+            // also tells the softmax that P·V_t(j-1) is done.
+            if (!(wait_kv(K(0)) && issue_s_safe(0, sm.ring(K(0))))) break;
+            if (n0 == 1) ptx::mma_commit(sm.q_empty(0));
+            for (int j = 0; j < n1; ++j) {
+                if (j >= 1) {
+                    if (!(wait_kv(V(j - 1)) && wait_p(1))) break;
+                    issue_pv(1, sm.ring(V(j - 1)), j > 1);
+                    ptx::mma_commit(sm.kv_empty(V(j - 1) % S));
+                }
+                if (!(wait_kv(K(j)) && issue_s_safe(1, sm.ring(K(j))))) break;
+                if (j == n1 - 1) ptx::mma_commit(sm.q_empty(1));
+                ptx::mma_commit(sm.kv_empty(K(j) % S));
                 if (j < n0) {
-                    if (!issue_s_safe(0, sm.ring(kj))) break;
-                    ptx::mma_commit(sm.s_full(0));
+                    if (!(wait_kv(V(j)) && wait_p(0))) break;
+                    issue_pv(0, sm.ring(V(j)), j > 0);
+                    if (j == n0 - 1) ptx::mma_commit(sm.o_full(0));
+                }
+                if (j + 1 < n0) {
+                    if (!(wait_kv(K(j + 1)) && issue_s_safe(0, sm.ring(K(j + 1))))) break;
+                    if (j + 1 == n0 - 1) ptx::mma_commit(sm.q_empty(0));
+                }
+            }
+            if (!ok) break;
+            if (!(wait_kv(V(n1 - 1)) && wait_p(1))) break;
+            issue_pv(1, sm.ring(V(n1 - 1)), n1 > 1);
+            ptx::mma_commit(sm.o_full(1));
+            ptx::mma_commit(sm.kv_empty(V(n1 - 1) % S));
+        } else {
+            // early S: S_t(j) needs only K_j and the softmax's read of S_t(j-1)
+            if (!(wait_kv(K(0)) && issue_s_safe(0, sm.ring(K(0))))) break;
+            if (n0 == 1) ptx::mma_commit(sm.q_empty(0));
+            if (!issue_s_safe(1, sm.ring(K(0)))) break;
+            if (n1 == 1) ptx::mma_commit(sm.q_empty(1));
+            ptx::mma_commit(sm.kv_empty(K(0) % S));
+            for (int j = 1; j < n1; ++j) {
+                if (!wait_kv(K(j))) break;
+                if (j < n0) {
+                    if (!issue_s_safe(0, sm.ring(K(j)))) break;
                     if (j == n0 - 1) ptx::mma_commit(sm.q_empty(0));
                 }
-                if (!issue_s_safe(1, sm.ring(kj))) break;
-                ptx::mma_commit(sm.s_full(1));
+                if (!issue_s_safe(1, sm.ring(K(j)))) break;
                 if (j == n1 - 1) ptx::mma_commit(sm.q_empty(1));
-                ptx::mma_commit(sm.kv_empty(kj % S));
-                if (!wait_kv(vprev)) break;
+                ptx::mma_commit(sm.kv_empty(K(j) % S));
+                if (!wait_kv(V(j - 1))) break;
                 if (j <= n0) {
                     if (!wait_p(0)) break;
-                    ptx::tc_fence_after_sync();
-                    issue_pv(0, sm.ring(vprev), j > 1);
+                    issue_pv(0, sm.ring(V(j - 1)), j > 1);
                     if (j == n0) ptx::mma_commit(sm.o_full(0));
                 }
                 if (!wait_p(1)) break;
-                ptx::tc_fence_after_sync();
-                issue_pv(1, sm.ring(vprev), j > 1);
-                ptx::mma_commit(sm.kv_empty(vprev % S));
-                continue;
+                issue_pv(1, sm.ring(V(j - 1)), j > 1);
+                ptx::mma_commit(sm.kv_empty(V(j - 1) % S));
             }
-            // P·V needs only V_{j-1}; K_j may still be in flight. (A second
-            // wait on K_j's slot is immediate: it is not refilled before release.)
-            if (!wait_kv(vprev)) break;
-            if (j <= n0) {
+            if (!ok) break;
+            if (!wait_kv(V(n1 - 1))) break;
+            if (n0 == n1) {
                 if (!wait_p(0)) break;
-                ptx::tc_fence_after_sync();
-                issue_pv(0, sm.ring(vprev), j > 1);
-                if (j < n0) {
-                    if (!wait_kv(kj)) break;
-                    if (!issue_s_safe(0, sm.ring(kj))) break;
-                    ptx::mma_commit(sm.s_full(0));
-                    if (j == n0 - 1) ptx::mma_commit(sm.q_empty(0));
-                } else {
-                    ptx::mma_commit(sm.o_full(0));
-                }
+                issue_pv(0, sm.ring(V(n1 - 1)), n1 > 1);
+                ptx::mma_commit(sm.o_full(0));
             }
             if (!wait_p(1)) break;
-            ptx::tc_fence_after_sync();
-            issue_pv(1, sm.ring(vprev), j > 1);
-            ptx::mma_commit(sm.kv_empty(vprev % S));
-            if (!wait_kv(kj)) break;
-            if (!issue_s_safe(1, sm.ring(kj))) break;
-            ptx::mma_commit(sm.s_full(1));
-            if (j == n1 - 1) ptx::mma_commit(sm.q_empty(1));
-            ptx::mma_commit(sm.kv_empty(kj % S));
+            issue_pv(1, sm.ring(V(n1 - 1)), n1 > 1);
+            ptx::mma_commit(sm.o_full(1));
+            ptx::mma_commit(sm.kv_empty(V(n1 - 1) % S));
         }
-        if (!ok) break;
-        // last key tile: P·V of the tiles still open
-        const uint32_t vlast = k0 + 2 * n1 - 1;
-        if (!wait_kv(vlast)) break;
-        if (n0 == n1) {
-            if (!wait_p(0)) break;
-            ptx::tc_fence_after_sync();
-            issue_pv(0, sm.ring(vlast), n1 > 1);
-            ptx::mma_commit(sm.o_full(0));
-        }
-        if (!wait_p(1)) break;
-        ptx::tc_fence_after_sync();
-        issue_pv(1, sm.ring(vlast), n1 > 1);
-        ptx::mma_commit(sm.o_full(1));
-        ptx::mma_commit(sm.kv_empty(vlast % S));
         kv_cnt = k0 + 2 * n1;
     }
 }
@@ -499,12 +484,10 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                     s[96 + i] = __uint_as_float(r3[i]);
                 }
             }
-            if (Cfg::kEarlyS) {
-                // S_t is in registers: the MMA warp may overwrite it with the next tile
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(sm.s_free(t));
-            }
+            // S is in registers: the MMA warp may write the next S into its buffer
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(sm.s_free(Cfg::kSharedS ? 0 : t));
             if (need_mask) {
 #pragma unroll
                 for (int c = 64; c < kBlockN; ++c) s[c] = (c > last) ? -INFINITY : s[c];
@@ -536,8 +519,8 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                 }
                 ptx::tc_fence_after_sync();
             }
-            // O_t *= alpha. (Without early S, the previous P·V of this tile
-            // finished before S_t was committed.)
+            // O_t *= alpha. (With the shared S buffer, the previous P·V of this
+            // tile was issued before S_t and finished before S_t was committed.)
             if (j > 0 && __any_sync(0xffffffffu, move)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 8; ++c) {
@@ -629,8 +612,8 @@ __global__ void __launch_bounds__(384, 1)
     using Cfg = WsCfg<D>;
     static_assert(D == 64 || D == 128, "head dim");
     // 384 threads launch with 168 registers each (64512); two softmax
-    // warpgroups at 216 and one control warpgroup at 72 use 55296 + 9216.
-    constexpr uint32_t kRegsSoftmax = 216, kRegsControl = 72;
+    // warpgroups at 200 and one control warpgroup at 104 use 51200 + 13312.
+    constexpr uint32_t kRegsSoftmax = 200, kRegsControl = 104;
     static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= 384 * 168, "register split");
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
