@@ -77,6 +77,14 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     return wait_slow(bar, parity, cta_abort, site, limit_ns);
 }
 
+// wait_phase for a whole converged warp: every lane polls, and the result is
+// made warp-uniform (false if any lane gave up).
+__device__ __forceinline__ bool wait_phase_warp(uint32_t bar, uint32_t parity, volatile int* cta_abort,
+                                                unsigned site, unsigned long long limit_ns) {
+    const bool ok = wait_phase(bar, parity, cta_abort, site, limit_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Final drain before TMEM is freed: waits for an mbarrier phase with a short
 // limit of its own, ignoring the abort flag (the point is to let any MMA still
 // in flight finish even after the CTA gave up on something else).

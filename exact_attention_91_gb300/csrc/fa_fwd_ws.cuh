@@ -176,17 +176,21 @@ struct WsGeometry {
 
 // ---------------------------------------------------------------- TMA producer
 template <int D, bool CAUSAL>
+// Run by the whole warp: addresses and coordinates stay warp-uniform and one
+// elected lane issues each copy.
 __device__ __forceinline__ void ws_load_role(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                             const CUtensorMap& tm_v, const FwdParams& p) {
+                                             const CUtensorMap& tm_v, const FwdParams& p, int lane) {
     using Cfg = WsCfg<D>;
     constexpr int S = Cfg::kStages;
     const WsSmem<D> sm;
     const WsGeometry g(p);
     volatile int* abort_flag = sm.abort_flag();
     const unsigned long long lim = p.wait_limit_ns;
-    ptx::prefetch_tensormap(&tm_q);
-    ptx::prefetch_tensormap(&tm_k);
-    ptx::prefetch_tensormap(&tm_v);
+    if (lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+    }
     const uint64_t keep = ptx::policy_evict_last();
     const uint64_t stream_once = ptx::policy_evict_first();
     constexpr int U = Cfg::kUnitSlots;
@@ -195,42 +199,51 @@ __device__ __forceinline__ void ws_load_role(const CUtensorMap& tm_q, const CUte
     for (int it = 0; ok; ++it) {
         // claim the next unit and hand it to the other roles
         const int qslot = it % U;
-        ok = wait_phase(sm.u_empty(qslot), ((it / U) & 1) ^ 1, abort_flag, kStatusTimeoutOther, lim);
+        ok = wait_phase_warp(sm.u_empty(qslot), ((it / U) & 1) ^ 1, abort_flag, kStatusTimeoutOther, lim);
         if (!ok) break;
-        int u = static_cast<int>(atomicAdd(p.sched, 1u));
-        if (u >= g.n_units) u = -1;
-        *sm.unit_slot(qslot) = u;
-        ptx::mbar_arrive(sm.u_full(qslot));
+        int u = 0;
+        if (lane == 0) {
+            u = static_cast<int>(atomicAdd(p.sched, 1u));
+            if (u >= g.n_units) u = -1;
+            *sm.unit_slot(qslot) = u;
+            ptx::mbar_arrive(sm.u_full(qslot));
+        }
+        u = __shfl_sync(0xffffffffu, u, 0);
         if (u < 0) break;
         int bh, qb;
         unit_coords(u, g.nqb, g.BH, bh, qb);
         const int n1 = kv_tiles_for<CAUSAL>(2 * qb + 1, g.n_k_tiles);
         for (int t = 0; t < 2 && ok; ++t) {
-            ok = wait_phase(sm.q_empty(t), (it & 1) ^ 1, abort_flag, kStatusTimeoutFree, lim);
+            ok = wait_phase_warp(sm.q_empty(t), (it & 1) ^ 1, abort_flag, kStatusTimeoutFree, lim);
             if (!ok) break;
-            ptx::mbar_arrive_expect_tx(sm.q_full(t), Cfg::kTileBytes);
+            ptx::mbar_arrive_expect_tx_elect(sm.q_full(t), Cfg::kTileBytes);
+#pragma unroll
             for (int c = 0; c < D / kBoxCols; ++c)
-                ptx::tma_load_3d_hint(sm.q_tile(t) + c * kBoxBytes, &tm_q, sm.q_full(t), c * kBoxCols,
-                                      qb * 2 * kBlockM + t * kBlockM, bh, stream_once);
+                ptx::tma_load_3d_hint_elect(sm.q_tile(t) + c * kBoxBytes, &tm_q, sm.q_full(t), c * kBoxCols,
+                                            qb * 2 * kBlockM + t * kBlockM, bh, stream_once);
         }
         for (int j = 0; j < n1 && ok; ++j) {
             for (int which = 0; which < 2; ++which, ++kv_cnt) {
                 const int slot = static_cast<int>(kv_cnt % S);
-                ok = wait_phase(sm.kv_empty(slot), ((kv_cnt / S) & 1) ^ 1, abort_flag, kStatusTimeoutFree, lim);
+                ok = wait_phase_warp(sm.kv_empty(slot), ((kv_cnt / S) & 1) ^ 1, abort_flag, kStatusTimeoutFree,
+                                     lim);
                 if (!ok) break;
-                ptx::mbar_arrive_expect_tx(sm.kv_full(slot), Cfg::kTileBytes);
+                ptx::mbar_arrive_expect_tx_elect(sm.kv_full(slot), Cfg::kTileBytes);
                 const CUtensorMap* map = which == 0 ? &tm_k : &tm_v;
+#pragma unroll
                 for (int c = 0; c < D / kBoxCols; ++c)
-                    ptx::tma_load_3d_hint(sm.ring(kv_cnt) + c * kBoxBytes, map, sm.kv_full(slot), c * kBoxCols,
-                                          j * kBlockN, bh, keep);
+                    ptx::tma_load_3d_hint_elect(sm.ring(kv_cnt) + c * kBoxBytes, map, sm.kv_full(slot),
+                                                c * kBoxCols, j * kBlockN, bh, keep);
             }
         }
     }
 }
 
 // ---------------------------------------------------------------- MMA issuer
+// Run by the whole warp: descriptors stay warp-uniform and one elected lane
+// issues each tcgen05.mma / tcgen05.commit.
 template <int D, bool CAUSAL>
-__device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
+__device__ __forceinline__ void ws_mma_role(const FwdParams& p, int lane) {
     using Cfg = WsCfg<D>;
     constexpr int S = Cfg::kStages;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, kBlockN, false, false);
@@ -249,7 +262,7 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-            ptx::mma_ss(tS, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
+            ptx::mma_ss_elect(tS, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
         }
     };
     // O_t += P_t·V over 128 keys in steps of 16 (2048 bytes of V each);
@@ -260,7 +273,7 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
         const uint32_t tO = tmem + (t == 0 ? Cfg::kTmemO0 : Cfg::kTmemO1);
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            ptx::mma_ts(tO, tP + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
+            ptx::mma_ts_elect(tO, tP + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
                         (accumulate || kk > 0) ? 1u : 0u);
         }
     };
@@ -274,7 +287,7 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
     auto issue_pv = [&](int t, uint32_t sV, bool accumulate) {
         ptx::tc_fence_after_sync();
         issue_pv_mma(t, sV, accumulate);
-        if (Cfg::kEarlyS) ptx::mma_commit(sm.pv_done(t));
+        if (Cfg::kEarlyS) ptx::mma_commit_elect(sm.pv_done(t));
     };
     // S_t = Q_t·K^T once its S buffer is free: the softmax has read every
     // earlier S written there.
@@ -283,28 +296,28 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
         uint32_t& seen = b == 0 ? sf_seen0 : sf_seen1;
         uint32_t& issued = b == 0 ? s_cnt0 : s_cnt1;
         while (ok && seen < issued) {
-            ok = wait_phase(sm.s_free(b), seen & 1, abort_flag, kStatusTimeoutSoftmax, lim);
+            ok = wait_phase_warp(sm.s_free(b), seen & 1, abort_flag, kStatusTimeoutSoftmax, lim);
             ++seen;
         }
         if (!ok) return false;
         ptx::tc_fence_after_sync();
         issue_s(t, sK);
         ++issued;
-        ptx::mma_commit(sm.s_full(t));
+        ptx::mma_commit_elect(sm.s_full(t));
         return true;
     };
     auto wait_p = [&](int t) {
         uint32_t& c = t == 0 ? p_cnt0 : p_cnt1;
-        ok = ok && wait_phase(sm.p_full(t), c & 1, abort_flag, kStatusTimeoutSoftmax, lim);
+        ok = ok && wait_phase_warp(sm.p_full(t), c & 1, abort_flag, kStatusTimeoutSoftmax, lim);
         ++c;
         return ok;
     };
     auto wait_kv = [&](uint32_t cnt) {
-        ok = ok && wait_phase(sm.kv_full(cnt % S), (cnt / S) & 1, abort_flag, kStatusTimeoutLoad, lim);
+        ok = ok && wait_phase_warp(sm.kv_full(cnt % S), (cnt / S) & 1, abort_flag, kStatusTimeoutLoad, lim);
         return ok;
     };
     for (int it = 0; ok; ++it) {
-        const int u = next_unit(sm, it, 0, 1u, p);
+        const int u = next_unit(sm, it, lane, 0xffffffffu, p);
         if (u < 0) break;
         int bh, qb;
         unit_coords(u, g.nqb, g.BH, bh, qb);
@@ -313,75 +326,75 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p) {
         const uint32_t k0 = kv_cnt;  // ring position of K_0; K_j = k0 + 2j, V_j = K_j + 1
         auto K = [&](int j) { return k0 + 2u * j; };
         auto V = [&](int j) { return k0 + 2u * j + 1u; };
-        if (!wait_phase(sm.q_full(0), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
-        if (!wait_phase(sm.q_full(1), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
+        if (!wait_phase_warp(sm.q_full(0), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
+        if (!wait_phase_warp(sm.q_full(1), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
         if (Cfg::kSharedS) {
             // TC order per key tile j: S0(j), PV1(j-1), S1(j), PV0(j). Each P·V
             // of a tile precedes that tile's next S, so the commit of S_t(j)
             // also tells the softmax that P·V_t(j-1) is done.
             if (!(wait_kv(K(0)) && issue_s_safe(0, sm.ring(K(0))))) break;
-            if (n0 == 1) ptx::mma_commit(sm.q_empty(0));
+            if (n0 == 1) ptx::mma_commit_elect(sm.q_empty(0));
             for (int j = 0; j < n1; ++j) {
                 if (j >= 1) {
                     if (!(wait_kv(V(j - 1)) && wait_p(1))) break;
                     issue_pv(1, sm.ring(V(j - 1)), j > 1);
-                    ptx::mma_commit(sm.kv_empty(V(j - 1) % S));
+                    ptx::mma_commit_elect(sm.kv_empty(V(j - 1) % S));
                 }
                 if (!(wait_kv(K(j)) && issue_s_safe(1, sm.ring(K(j))))) break;
-                if (j == n1 - 1) ptx::mma_commit(sm.q_empty(1));
-                ptx::mma_commit(sm.kv_empty(K(j) % S));
+                if (j == n1 - 1) ptx::mma_commit_elect(sm.q_empty(1));
+                ptx::mma_commit_elect(sm.kv_empty(K(j) % S));
                 if (j < n0) {
                     if (!(wait_kv(V(j)) && wait_p(0))) break;
                     issue_pv(0, sm.ring(V(j)), j > 0);
-                    if (j == n0 - 1) ptx::mma_commit(sm.o_full(0));
+                    if (j == n0 - 1) ptx::mma_commit_elect(sm.o_full(0));
                 }
                 if (j + 1 < n0) {
                     if (!(wait_kv(K(j + 1)) && issue_s_safe(0, sm.ring(K(j + 1))))) break;
-                    if (j + 1 == n0 - 1) ptx::mma_commit(sm.q_empty(0));
+                    if (j + 1 == n0 - 1) ptx::mma_commit_elect(sm.q_empty(0));
                 }
             }
             if (!ok) break;
             if (!(wait_kv(V(n1 - 1)) && wait_p(1))) break;
             issue_pv(1, sm.ring(V(n1 - 1)), n1 > 1);
-            ptx::mma_commit(sm.o_full(1));
-            ptx::mma_commit(sm.kv_empty(V(n1 - 1) % S));
+            ptx::mma_commit_elect(sm.o_full(1));
+            ptx::mma_commit_elect(sm.kv_empty(V(n1 - 1) % S));
         } else {
             // early S: S_t(j) needs only K_j and the softmax's read of S_t(j-1)
             if (!(wait_kv(K(0)) && issue_s_safe(0, sm.ring(K(0))))) break;
-            if (n0 == 1) ptx::mma_commit(sm.q_empty(0));
+            if (n0 == 1) ptx::mma_commit_elect(sm.q_empty(0));
             if (!issue_s_safe(1, sm.ring(K(0)))) break;
-            if (n1 == 1) ptx::mma_commit(sm.q_empty(1));
-            ptx::mma_commit(sm.kv_empty(K(0) % S));
+            if (n1 == 1) ptx::mma_commit_elect(sm.q_empty(1));
+            ptx::mma_commit_elect(sm.kv_empty(K(0) % S));
             for (int j = 1; j < n1; ++j) {
                 if (!wait_kv(K(j))) break;
                 if (j < n0) {
                     if (!issue_s_safe(0, sm.ring(K(j)))) break;
-                    if (j == n0 - 1) ptx::mma_commit(sm.q_empty(0));
+                    if (j == n0 - 1) ptx::mma_commit_elect(sm.q_empty(0));
                 }
                 if (!issue_s_safe(1, sm.ring(K(j)))) break;
-                if (j == n1 - 1) ptx::mma_commit(sm.q_empty(1));
-                ptx::mma_commit(sm.kv_empty(K(j) % S));
+                if (j == n1 - 1) ptx::mma_commit_elect(sm.q_empty(1));
+                ptx::mma_commit_elect(sm.kv_empty(K(j) % S));
                 if (!wait_kv(V(j - 1))) break;
                 if (j <= n0) {
                     if (!wait_p(0)) break;
                     issue_pv(0, sm.ring(V(j - 1)), j > 1);
-                    if (j == n0) ptx::mma_commit(sm.o_full(0));
+                    if (j == n0) ptx::mma_commit_elect(sm.o_full(0));
                 }
                 if (!wait_p(1)) break;
                 issue_pv(1, sm.ring(V(j - 1)), j > 1);
-                ptx::mma_commit(sm.kv_empty(V(j - 1) % S));
+                ptx::mma_commit_elect(sm.kv_empty(V(j - 1) % S));
             }
             if (!ok) break;
             if (!wait_kv(V(n1 - 1))) break;
             if (n0 == n1) {
                 if (!wait_p(0)) break;
                 issue_pv(0, sm.ring(V(n1 - 1)), n1 > 1);
-                ptx::mma_commit(sm.o_full(0));
+                ptx::mma_commit_elect(sm.o_full(0));
             }
             if (!wait_p(1)) break;
             issue_pv(1, sm.ring(V(n1 - 1)), n1 > 1);
-            ptx::mma_commit(sm.o_full(1));
-            ptx::mma_commit(sm.kv_empty(V(n1 - 1) % S));
+            ptx::mma_commit_elect(sm.o_full(1));
+            ptx::mma_commit_elect(sm.kv_empty(V(n1 - 1) % S));
         }
         kv_cnt = k0 + 2 * n1;
     }
@@ -642,10 +655,10 @@ __global__ void __launch_bounds__(384, 1)
         ptx::named_bar_sync(Cfg::kBarAll, Cfg::kThreads);
         ptx::tc_fence_after_sync();
         if (warp == 9) {
-            if (lane == 0) ws_load_role<D, CAUSAL>(tm_q, tm_k, tm_v, p);
+            ws_load_role<D, CAUSAL>(tm_q, tm_k, tm_v, p, lane);
             __syncwarp();
         } else if (warp == 8) {
-            if (lane == 0) ws_mma_role<D, CAUSAL>(p);
+            ws_mma_role<D, CAUSAL>(p, lane);
             __syncwarp();
         }
         ptx::tc_fence_before_sync();
