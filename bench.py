@@ -199,21 +199,24 @@ class OracleSampler:
         self.sec_per_flop = None
 
     def run(self, target_s: float):
-        """One timed sample sized to take about target_s seconds.
-        Returns (flops, seconds, rows)."""
+        """Random rows timed in batches until about target_s seconds of
+        oracle work have been done. Returns (flops, seconds, rows)."""
         w = self.w
-        if self.sec_per_flop is None:
-            probe = self.g.integers(0, self.n_local, size=min(self.n_local, 32))
+        flops = secs = 0.0
+        rows_done = 0
+        batch = 16
+        while secs < target_s and rows_done < 50 * self.n_local:
+            rows = self.g.integers(0, self.n_local, size=batch)
             t = time.perf_counter()
-            self.oracle.attn_rows(self.q, self.k, self.v, probe, w.scale, w.causal)
-            self.sec_per_flop = max(time.perf_counter() - t, 1e-6) / max(row_flops(w, probe), 1.0)
-        avg_row = 4.0 * w.d * (w.N + 1) / 2 if w.causal else 4.0 * w.d * w.N
-        n = int(min(self.n_local, max(16, target_s / (self.sec_per_flop * avg_row))))
-        rows = self.g.integers(0, self.n_local, size=n)
-        t = time.perf_counter()
-        self.oracle.attn_rows(self.q, self.k, self.v, rows, w.scale, w.causal)
-        dt = time.perf_counter() - t
-        return row_flops(w, rows), dt, n
+            self.oracle.attn_rows(self.q, self.k, self.v, rows, w.scale, w.causal)
+            dt = time.perf_counter() - t
+            flops += row_flops(w, rows)
+            secs += dt
+            rows_done += batch
+            # next batch sized to about a quarter of what is left
+            per_row = dt / batch
+            batch = int(max(16, min(self.n_local, 0.25 * (target_s - secs) / max(per_row, 1e-9))))
+        return flops, secs, rows_done
 
     def describe(self, n_rows: int, seconds: float) -> str:
         return (f"{n_rows} random query rows from {len(self.heads)} heads of the {self.w.name} workload "
