@@ -37,6 +37,7 @@ struct DeviceState {
     int sm_count = 0;
     unsigned* sched = nullptr;  // kSchedSlots x kSchedSlotWords, allocated on first use
     std::atomic<unsigned> sched_next{0};
+    cudaMemPool_t pool = nullptr;  // stream-ordered scratch for key-range splits
 };
 DeviceState g_devices[kMaxDevices];
 
@@ -104,6 +105,49 @@ int probe_device(int* dev_out, DeviceState** st_out) {
     return st.status;
 }
 
+// The device's pool for per-call split scratch: stream-ordered, so calls on
+// different streams never share it, and it keeps its memory between calls.
+int ensure_pool(int dev, DeviceState& st) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (st.pool) return FA_OK;
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_LAUNCH;
+    }
+    unsigned long long keep = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    st.pool = pool;
+    return FA_OK;
+}
+
+// Number of splits of each unit's key range: only without the causal mask
+// (whose units differ in size and balance through the work queue), only
+// while each split keeps at least 4 key tiles, and only when it raises the
+// share of busy CTA slots in the last wave by more than 3 points.
+int choose_nsplit(long long units, int n_k_tiles, int sms, bool causal) {
+    if (causal || sms <= 0) return 1;
+    auto eff = [&](long long items) {
+        const long long waves = (items + sms - 1) / sms;
+        return static_cast<double>(items) / static_cast<double>(waves * sms);
+    };
+    int best = 1;
+    double best_eff = eff(units);
+    for (int sp = 2; sp <= 4; ++sp) {
+        if (n_k_tiles / sp < 4) break;
+        const double e = eff(units * sp);
+        if (e > best_eff + 0.03) {
+            best = sp;
+            best_eff = e;
+        }
+    }
+    return best;
+}
+
 // 3-D view [B*H][N][d] of a contiguous bf16 [B,H,N,d] tensor, boxes of
 // 128 rows x 64 columns (128 bytes, 128-byte swizzle). Rows past N inside a
 // head read as zero and are not written by stores.
@@ -167,20 +211,24 @@ int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
         }
     }
     const long long nqb = (static_cast<long long>(prm.N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-    const long long units = nqb * prm.num_heads_total;
-    const unsigned grid = static_cast<unsigned>(units < sm_count ? units : sm_count);
+    const long long items = nqb * prm.num_heads_total * (prm.nsplit > 1 ? prm.nsplit : 1);
+    const unsigned grid = static_cast<unsigned>(items < sm_count ? items : sm_count);
     kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+bool use_simple_kernel() {
+    static const bool use_simple = [] {
+        const char* e = std::getenv("FA_KERNEL");
+        return e != nullptr && e[0] == 's';
+    }();
+    return use_simple;
 }
 
 template <int D, bool CAUSAL>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
            const fa::FwdParams& prm, int dev, int sm_count, cudaStream_t stream) {
-    static const bool use_simple = [] {
-        const char* e = std::getenv("FA_KERNEL");
-        return e != nullptr && e[0] == 's';
-    }();
-    if (use_simple) return launch_simple<D, CAUSAL>(tq, tk, tv, to, prm, dev, stream);
+    if (use_simple_kernel()) return launch_simple<D, CAUSAL>(tq, tk, tv, to, prm, dev, stream);
     return launch_ws<D, CAUSAL>(tq, tk, tv, to, prm, dev, sm_count, stream);
 }
 
@@ -274,10 +322,40 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     prm.sched = st->sched + (st->sched_next.fetch_add(1) % kSchedSlots) * kSchedSlotWords;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int sms = st->sm_count;
+    const long long units = ((static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM)) * BH;
+    const int n_k_tiles = static_cast<int>((static_cast<long long>(N) + fa::kBlockN - 1) / fa::kBlockN);
+    prm.nsplit = use_simple_kernel() ? 1 : choose_nsplit(units, n_k_tiles, sms, causal != 0);
+    void* scratch = nullptr;
+    if (prm.nsplit > 1) {
+        // per call, stream-ordered: [partial O | partial LSE | tickets]
+        const size_t items = static_cast<size_t>(units) * prm.nsplit;
+        const size_t o_bytes = items * 2 * fa::kBlockM * d * sizeof(float);
+        const size_t l_bytes = items * 2 * fa::kBlockM * sizeof(float);
+        const size_t t_bytes = static_cast<size_t>(units) * 2 * sizeof(unsigned);
+        if (ensure_pool(dev, *st) != FA_OK ||
+            cudaMallocFromPoolAsync(&scratch, o_bytes + l_bytes + t_bytes, st->pool, s) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_LAUNCH;
+        }
+        prm.part_o = static_cast<float*>(scratch);
+        prm.part_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
+        prm.tickets = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + o_bytes + l_bytes);
+        if (cudaMemsetAsync(prm.tickets, 0, t_bytes, s) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFreeAsync(scratch, s);
+            return FA_ERR_LAUNCH;
+        }
+    }
     if (d == 64)
-        return causal ? launch<64, true>(tq, tk, tv, to, prm, dev, sms, s) : launch<64, false>(tq, tk, tv, to, prm, dev, sms, s);
-    return causal ? launch<128, true>(tq, tk, tv, to, prm, dev, sms, s)
-                  : launch<128, false>(tq, tk, tv, to, prm, dev, sms, s);
+        rc = causal ? launch<64, true>(tq, tk, tv, to, prm, dev, sms, s) : launch<64, false>(tq, tk, tv, to, prm, dev, sms, s);
+    else
+        rc = causal ? launch<128, true>(tq, tk, tv, to, prm, dev, sms, s)
+                    : launch<128, false>(tq, tk, tv, to, prm, dev, sms, s);
+    if (scratch && cudaFreeAsync(scratch, s) != cudaSuccess) {
+        cudaGetLastError();
+        if (rc == FA_OK) rc = FA_ERR_LAUNCH;
+    }
+    return rc;
 }
 
 }  // extern "C"
@@ -372,6 +450,7 @@ extern "C" int fa_fwd_noalloc(const void* q, const void* k, const void* v, void*
         prm.wait_limit_ns = g_wait_limit_ns;
     }
     prm.sched = scratch;
+    prm.nsplit = 1;  // no key-range split: its partial results would need more scratch
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the two counters must start at zero (the kernel also leaves them zero)
     if (cudaMemsetAsync(scratch, 0, 2 * sizeof(unsigned), s) != cudaSuccess) {

@@ -36,6 +36,13 @@ struct FwdParams {
     float scale_log2;     // scale * log2(e): scores are kept in base-2 units
     unsigned long long wait_limit_ns;  // give up on an mbarrier wait after this long
     unsigned* sched;      // work-queue slot {next unit, CTAs finished}; zero at launch, zero again at exit
+    // Key-range split (non-causal problems with few work units): each unit's
+    // key tiles are divided among `nsplit` work items whose partial results
+    // are merged by the last one to finish. nsplit = 1: no scratch is used.
+    int nsplit;
+    float* part_o;        // [items][2 tiles][d/4][128 rows][4] fp32: normalised partial O
+    float* part_lse;      // [items][2 tiles][128 rows] fp32: base-2 log-sum-exp of each partial
+    unsigned* tickets;    // [units][2 tiles], zero at launch: splits of a tile finished so far
 };
 
 // Device-wide status word (one per device that loads the library). Zero means

@@ -64,7 +64,7 @@ struct WsCfg {
     //           u_full[U] u_empty[U] pv_done[2] s_free[2]
     static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 * kUnitSlots + 2 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit queue
-    static constexpr int kSmemBytes = kOffMisc + 8 + 4 * kUnitSlots + 1024;  // + base alignment slack
+    static constexpr int kSmemBytes = kOffMisc + 8 + 4 * kUnitSlots + 8 + 1024;  // + base alignment slack
     // arrivals that free a unit-queue slot: the MMA thread and the 8 softmax warps
     static constexpr uint32_t kUnitConsumers = 9;
     static constexpr int kTmemCols = 512;
@@ -112,6 +112,10 @@ struct WsSmem {
     __device__ __forceinline__ uint32_t s_free(int t) const { return bar(13 + 2 * S + 2 * Cfg::kUnitSlots + t); }
     __device__ __forceinline__ volatile int* unit_slot(int i) const {
         return reinterpret_cast<volatile int*>(base + Cfg::kOffMisc + 8) + i;
+    }
+    // per softmax warpgroup: "this split is the last of its tile" flag
+    __device__ __forceinline__ volatile int* last_flag(int t) const {
+        return reinterpret_cast<volatile int*>(base + Cfg::kOffMisc + 8 + 4 * Cfg::kUnitSlots) + t;
     }
     __device__ __forceinline__ uint32_t* tmem_slot() const {
         return reinterpret_cast<uint32_t*>(base + Cfg::kOffMisc);
@@ -165,14 +169,40 @@ __device__ __forceinline__ int next_unit(const WsSmem<D>& sm, int it, int lane, 
 }
 
 struct WsGeometry {
-    int BH, n_k_tiles, nqb, n_units;
+    int BH, n_k_tiles, nqb, n_units, nsplit, n_items;
     __device__ __forceinline__ explicit WsGeometry(const FwdParams& p) {
         BH = p.num_heads_total;
         n_k_tiles = (p.N + kBlockN - 1) / kBlockN;
         nqb = (p.N + 2 * kBlockM - 1) / (2 * kBlockM);
         n_units = nqb * BH;
+        nsplit = p.nsplit;
+        n_items = n_units * nsplit;
     }
 };
+
+// A work item: one unit (head, 256-row block) and, when the key range is
+// split, one contiguous share of its key tiles: tiles jb .. jb+n1-1 (tile 0
+// of the unit sees n0 of them, n0 <= n1 <= n0 + 1 under the causal mask).
+struct WsItem {
+    int unit, split, bh, qb, jb, n0, n1;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ WsItem item_coords(int item, const WsGeometry& g) {
+    WsItem w;
+    w.unit = item / g.nsplit;
+    w.split = item - w.unit * g.nsplit;
+    unit_coords(w.unit, g.nqb, g.BH, w.bh, w.qb);
+    if (CAUSAL || g.nsplit == 1) {
+        w.jb = 0;
+        w.n0 = kv_tiles_for<CAUSAL>(2 * w.qb, g.n_k_tiles);
+        w.n1 = kv_tiles_for<CAUSAL>(2 * w.qb + 1, g.n_k_tiles);
+    } else {
+        w.jb = w.split * g.n_k_tiles / g.nsplit;
+        w.n0 = w.n1 = (w.split + 1) * g.n_k_tiles / g.nsplit - w.jb;
+    }
+    return w;
+}
 
 // ---------------------------------------------------------------- TMA producer
 template <int D, bool CAUSAL>
@@ -204,15 +234,14 @@ __device__ __forceinline__ void ws_load_role(const CUtensorMap& tm_q, const CUte
         int u = 0;
         if (lane == 0) {
             u = static_cast<int>(atomicAdd(p.sched, 1u));
-            if (u >= g.n_units) u = -1;
+            if (u >= g.n_items) u = -1;
             *sm.unit_slot(qslot) = u;
             ptx::mbar_arrive(sm.u_full(qslot));
         }
         u = __shfl_sync(0xffffffffu, u, 0);
         if (u < 0) break;
-        int bh, qb;
-        unit_coords(u, g.nqb, g.BH, bh, qb);
-        const int n1 = kv_tiles_for<CAUSAL>(2 * qb + 1, g.n_k_tiles);
+        const WsItem w = item_coords<CAUSAL>(u, g);
+        const int bh = w.bh, qb = w.qb, n1 = w.n1;
         for (int t = 0; t < 2 && ok; ++t) {
             ok = wait_phase_warp(sm.q_empty(t), (it & 1) ^ 1, abort_flag, kStatusTimeoutFree, lim);
             if (!ok) break;
@@ -233,7 +262,7 @@ __device__ __forceinline__ void ws_load_role(const CUtensorMap& tm_q, const CUte
 #pragma unroll
                 for (int c = 0; c < D / kBoxCols; ++c)
                     ptx::tma_load_3d_hint_elect(sm.ring(kv_cnt) + c * kBoxBytes, map, sm.kv_full(slot),
-                                                c * kBoxCols, j * kBlockN, bh, keep);
+                                                c * kBoxCols, (w.jb + j) * kBlockN, bh, keep);
             }
         }
     }
@@ -319,10 +348,8 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p, int lane) {
     for (int it = 0; ok; ++it) {
         const int u = next_unit(sm, it, lane, 0xffffffffu, p);
         if (u < 0) break;
-        int bh, qb;
-        unit_coords(u, g.nqb, g.BH, bh, qb);
-        const int n0 = kv_tiles_for<CAUSAL>(2 * qb, g.n_k_tiles);
-        const int n1 = kv_tiles_for<CAUSAL>(2 * qb + 1, g.n_k_tiles);  // n0 <= n1 <= n0 + 1
+        const WsItem w = item_coords<CAUSAL>(u, g);
+        const int n0 = w.n0, n1 = w.n1;  // n0 <= n1 <= n0 + 1
         const uint32_t k0 = kv_cnt;  // ring position of K_0; K_j = k0 + 2j, V_j = K_j + 1
         auto K = [&](int j) { return k0 + 2u * j; };
         auto V = [&](int j) { return k0 + 2u * j + 1u; };
@@ -440,11 +467,11 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
         const int u = next_unit(sm, it, lane, 0xffffffffu, p);
         if (u == -2) failed = true;
         if (named_bar_or(1 + t, 128, u < 0)) break;  // the warpgroup agrees on stopping
-        int bh, qb;
-        unit_coords(u, g.nqb, g.BH, bh, qb);
-        const int q_tile = 2 * qb + t;
+        const WsItem w = item_coords<CAUSAL>(u, g);
+        const int bh = w.bh;
+        const int q_tile = 2 * w.qb + t;
         const int i0 = q_tile * kBlockM;
-        const int n_t = kv_tiles_for<CAUSAL>(q_tile, g.n_k_tiles);
+        const int n_t = t == 0 ? w.n0 : w.n1;
         float m_ref = -INFINITY;  // reference max (base 2) that O and l are relative to
         float l = 0.f;
         for (int j = 0; j < n_t; ++j) {
@@ -458,10 +485,11 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
             // this thread's row of S: the max of the first half overlaps the load of the second
             float s[kBlockN];
             float mx0, mx1, mx2, mx3;
-            const int key0 = j * kBlockN;
-            const bool need_mask = key0 + kBlockN > p.N || (CAUSAL && j == q_tile);
+            const int jt = w.jb + j;  // key tile index within the head
+            const int key0 = jt * kBlockN;
+            const bool need_mask = key0 + kBlockN > p.N || (CAUSAL && jt == q_tile);
             int last = p.N - 1 - key0;  // last visible column of this tile
-            if (CAUSAL && j == q_tile) last = min(last, row);
+            if (CAUSAL && jt == q_tile) last = min(last, row);
             {
                 uint32_t r0[32], r1[32], r2[32], r3[32];
                 ptx::tmem_ld_32x32b_x32(tS + 0, r0);
@@ -585,19 +613,18 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
         }
         ptx::tc_fence_after_sync();
         const float inv_l = 1.0f / l;
-#pragma unroll
-        for (int b = 0; b < D / kBoxCols; ++b) {
-            float o[64];
-            load_row64(tO + b * 64, o);
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float lse2 = m_use + log2f(l);  // base-2 log-sum-exp of this row's scaled scores
+        // one 64-column box of the final O (fp32 row values f[0..63]) -> bf16 -> staging -> TMA store
+        auto store_box = [&](int b, const float (&f)[64]) {
 #pragma unroll
             for (int q8 = 0; q8 < 8; ++q8) {
-                const float* f = o + q8 * 8;
-                uint4 w;
-                w.x = ptx::pack_bf16x2(f[0] * inv_l, f[1] * inv_l);
-                w.y = ptx::pack_bf16x2(f[2] * inv_l, f[3] * inv_l);
-                w.z = ptx::pack_bf16x2(f[4] * inv_l, f[5] * inv_l);
-                w.w = ptx::pack_bf16x2(f[6] * inv_l, f[7] * inv_l);
-                *reinterpret_cast<uint4*>(stage + sw128_offset(row, q8)) = w;
+                uint4 v;
+                v.x = ptx::pack_bf16x2(f[q8 * 8 + 0], f[q8 * 8 + 1]);
+                v.y = ptx::pack_bf16x2(f[q8 * 8 + 2], f[q8 * 8 + 3]);
+                v.z = ptx::pack_bf16x2(f[q8 * 8 + 4], f[q8 * 8 + 5]);
+                v.w = ptx::pack_bf16x2(f[q8 * 8 + 6], f[q8 * 8 + 7]);
+                *reinterpret_cast<uint4*>(stage + sw128_offset(row, q8)) = v;
             }
             ptx::fence_proxy_async_smem();
             ptx::named_bar_sync(1 + t, 128);
@@ -607,11 +634,77 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                 ptx::bulk_wait_group_read0();
             }
             ptx::named_bar_sync(1 + t, 128);
+        };
+        bool write_out = true;
+        if (g.nsplit > 1) {
+            // Split key range: publish this split's normalised O and LSE, take a
+            // ticket, and let the last split of the tile merge all of them.
+            const size_t slot = static_cast<size_t>(u) * 2 + t;  // (item, tile)
+            float* po = p.part_o + slot * (D / 4) * kBlockM * 4;
+#pragma unroll
+            for (int b = 0; b < D / kBoxCols; ++b) {
+                float o[64];
+                load_row64(tO + b * 64, o);
+#pragma unroll
+                for (int cg = 0; cg < 16; ++cg)
+                    *reinterpret_cast<float4*>(po + ((b * 16 + cg) * kBlockM + row) * 4) =
+                        make_float4(o[cg * 4] * inv_l, o[cg * 4 + 1] * inv_l, o[cg * 4 + 2] * inv_l,
+                                    o[cg * 4 + 3] * inv_l);
+            }
+            p.part_lse[slot * kBlockM + row] = lse2;
+            __threadfence();
+            ptx::named_bar_sync(1 + t, 128);
+            if (row == 0) {
+                const unsigned done = atomicAdd(p.tickets + static_cast<size_t>(w.unit) * 2 + t, 1u);
+                *sm.last_flag(t) = (done == static_cast<unsigned>(g.nsplit - 1)) ? 1 : 0;
+            }
+            ptx::named_bar_sync(1 + t, 128);
+            write_out = *sm.last_flag(t) != 0;
+            if (write_out) {
+                __threadfence();
+                // merge: O = sum_s 2^(L_s - M) O_s / sum_s 2^(L_s - M), LSE = M + log2(sum)
+                const size_t first = static_cast<size_t>(w.unit) * g.nsplit * 2 + t;  // slot of split 0
+                float mmax = -INFINITY;
+                for (int sp = 0; sp < g.nsplit; ++sp)
+                    mmax = fmaxf(mmax, p.part_lse[(first + 2 * sp) * kBlockM + row]);
+                float wsum = 0.f;
+                for (int sp = 0; sp < g.nsplit; ++sp)
+                    wsum += ptx::ex2_approx(p.part_lse[(first + 2 * sp) * kBlockM + row] - mmax);
+                const float inv_w = 1.0f / wsum;
+#pragma unroll 1
+                for (int b = 0; b < D / kBoxCols; ++b) {
+                    float acc[64];
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+                    for (int sp = 0; sp < g.nsplit; ++sp) {
+                        const float wgt =
+                            ptx::ex2_approx(p.part_lse[(first + 2 * sp) * kBlockM + row] - mmax) * inv_w;
+                        const float* ps = p.part_o + (first + 2 * sp) * (D / 4) * kBlockM * 4;
+#pragma unroll
+                        for (int cg = 0; cg < 16; ++cg) {
+                            const float4 v = *reinterpret_cast<const float4*>(ps + ((b * 16 + cg) * kBlockM + row) * 4);
+                            acc[cg * 4] = fmaf(wgt, v.x, acc[cg * 4]);
+                            acc[cg * 4 + 1] = fmaf(wgt, v.y, acc[cg * 4 + 1]);
+                            acc[cg * 4 + 2] = fmaf(wgt, v.z, acc[cg * 4 + 2]);
+                            acc[cg * 4 + 3] = fmaf(wgt, v.w, acc[cg * 4 + 3]);
+                        }
+                    }
+                    store_box(b, acc);
+                }
+                lse2 = mmax + log2f(wsum);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < D / kBoxCols; ++b) {
+                float o[64];
+                load_row64(tO + b * 64, o);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) o[i] *= inv_l;
+                store_box(b, o);
+            }
         }
-        if (p.lse != nullptr && i0 + row < p.N) {
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            p.lse[static_cast<size_t>(bh) * p.N + i0 + row] = (m_use + log2f(l)) * 0.69314718055994531f;
-        }
+        if (write_out && p.lse != nullptr && i0 + row < p.N)
+            p.lse[static_cast<size_t>(bh) * p.N + i0 + row] = lse2 * 0.69314718055994531f;
         ptx::tc_fence_before_sync();
     }
     if (row == 0) ptx::bulk_wait_group0();
