@@ -9,10 +9,13 @@
 // Roles (12 warps):
 //   warps 0-3  softmax of tile 0    (one query row per thread, TMEM lanes 0-127)
 //   warps 4-7  softmax of tile 1
-//   warp  8    MMA issue (one thread) and TMEM allocation
-//   warp  9    TMA loads (one thread) and barrier initialisation
-//   warps 10-11 idle (they complete the control warpgroup, which gives its
-//              registers to the softmax warpgroups)
+//   warp  8    issues every S = Q·Kᵀ MMA; TMEM allocation
+//   warp  9    TMA loads and barrier initialisation
+//   warp  10   issues the P·V MMAs of tile 0
+//   warp  11   issues the P·V MMAs of tile 1
+// (warps 8-11 form the control warpgroup, which gives registers to the
+// softmax warpgroups; each control warp runs its loop as a whole warp and one
+// elected lane issues each copy or MMA)
 // The roles are chosen before anything else runs, so no value is live across
 // the register split; each role derives its addresses from the kernel
 // parameters and shared memory.
@@ -60,13 +63,11 @@ struct WsCfg {
     static constexpr int kOffStage = kOffRing + kStages * kTileBytes;  // O staging, one box per tile
     static constexpr int kOffBar = kOffStage + 2 * kBoxBytes;
     static constexpr int kUnitSlots = 4;                     // work units handed from the TMA thread to the others
-    // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] fin
+    // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] fin[3]
     //           u_full[U] u_empty[U] pv_done[2] s_free[2]
-    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2 * kUnitSlots + 2 + 2;
+    static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 3 + 2 * kUnitSlots + 2 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit queue
     static constexpr int kSmemBytes = kOffMisc + 8 + 4 * kUnitSlots + 8 + 1024;  // + base alignment slack
-    // arrivals that free a unit-queue slot: the MMA thread and the 8 softmax warps
-    static constexpr uint32_t kUnitConsumers = 9;
     static constexpr int kTmemCols = 512;
     // TMEM columns. P (bf16 pairs, 64 columns per tile) never overlays S, so
     // no MMA that writes S can race a P·V that is still reading P: tcgen05.mma
@@ -74,9 +75,10 @@ struct WsCfg {
     //  d = 128: one S buffer shared by the two tiles, used alternately (each
     //           softmax copies S into registers at once); P0, P1, O0, O1.
     //  d = 64:  an S buffer per tile, so S_t(j+1) can be computed as soon as
-    //           the softmax has read S_t(j) ("early S"); P0, P1, O0, O1.
+    //           the softmax has read S_t(j); P0, P1, O0, O1.
     static constexpr bool kSharedS = D == 128;
-    static constexpr bool kEarlyS = !kSharedS;
+    // arrivals that free a unit-queue slot: the 3 MMA-issuing warps and the 8 softmax warps
+    static constexpr uint32_t kUnitConsumers = 11;
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = kSharedS ? 0 : 128;
     static constexpr uint32_t kTmemP0 = kSharedS ? 128 : 384, kTmemP1 = kSharedS ? 192 : 448;
     static constexpr uint32_t kTmemO0 = 256, kTmemO1 = 256 + D;
@@ -105,11 +107,11 @@ struct WsSmem {
     __device__ __forceinline__ uint32_t s_full(int t) const { return bar(4 + 2 * S + t); }
     __device__ __forceinline__ uint32_t p_full(int t) const { return bar(6 + 2 * S + t); }
     __device__ __forceinline__ uint32_t o_full(int t) const { return bar(8 + 2 * S + t); }
-    __device__ __forceinline__ uint32_t fin() const { return bar(10 + 2 * S); }
-    __device__ __forceinline__ uint32_t u_full(int i) const { return bar(11 + 2 * S + i); }
-    __device__ __forceinline__ uint32_t u_empty(int i) const { return bar(11 + 2 * S + Cfg::kUnitSlots + i); }
-    __device__ __forceinline__ uint32_t pv_done(int t) const { return bar(11 + 2 * S + 2 * Cfg::kUnitSlots + t); }
-    __device__ __forceinline__ uint32_t s_free(int t) const { return bar(13 + 2 * S + 2 * Cfg::kUnitSlots + t); }
+    __device__ __forceinline__ uint32_t fin(int m) const { return bar(10 + 2 * S + m); }
+    __device__ __forceinline__ uint32_t u_full(int i) const { return bar(13 + 2 * S + i); }
+    __device__ __forceinline__ uint32_t u_empty(int i) const { return bar(13 + 2 * S + Cfg::kUnitSlots + i); }
+    __device__ __forceinline__ uint32_t pv_done(int t) const { return bar(13 + 2 * S + 2 * Cfg::kUnitSlots + t); }
+    __device__ __forceinline__ uint32_t s_free(int t) const { return bar(15 + 2 * S + 2 * Cfg::kUnitSlots + t); }
     __device__ __forceinline__ volatile int* unit_slot(int i) const {
         return reinterpret_cast<volatile int*>(base + Cfg::kOffMisc + 8) + i;
     }
@@ -151,7 +153,7 @@ __device__ __forceinline__ int kv_tiles_for(int q_tile, int n_k_tiles) {
 
 // Next unit of this CTA from the unit queue (consumer side): waits for queue
 // slot `it`, reads it, and frees the slot. `mask` names the calling lanes of
-// the warp (all 32 for a softmax warp, lane 0 alone for the MMA thread); the
+// the warp (all 32 for every caller here); the
 // lowest of them arrives once after all have read. Returns -1 when the CTA has
 // no more work, and -2 if the wait gave up.
 template <int D>
@@ -268,21 +270,31 @@ __device__ __forceinline__ void ws_load_role(const CUtensorMap& tm_q, const CUte
     }
 }
 
-// ---------------------------------------------------------------- MMA issuer
-// Run by the whole warp: descriptors stay warp-uniform and one elected lane
-// issues each tcgen05.mma / tcgen05.commit.
+// ---------------------------------------------------------------- MMA issuers
+// Three warps issue the tcgen05.mma work: one issues every S = Q·Kᵀ (both
+// tiles, in the order S0(0), S1(0), S0(1), S1(1), ...), and one per tile
+// issues that tile's O += P·V. Issuing a tcgen05.mma costs the issuing warp
+// tens of cycles, so one warp alone cannot keep the tensor core busy while it
+// also waits on the softmax; split three ways, each warp's share of the issue
+// and barrier work fits in the time the tensor core spends on its MMAs.
+// Every warp runs its loop whole: descriptors stay warp-uniform and one
+// elected lane issues each tcgen05.mma / tcgen05.commit.
+
+// S_t = Q_t·K_jᵀ for both tiles, one key tile after the other. An S buffer is
+// rewritten only after the softmax has read (s_free) everything written there
+// before; with d = 128 both tiles share one buffer, so S1(j) follows the read
+// of S0(j) and S0(j+1) the read of S1(j). K slots are released here.
 template <int D, bool CAUSAL>
-__device__ __forceinline__ void ws_mma_role(const FwdParams& p, int lane) {
+__device__ __forceinline__ void ws_s_role(const FwdParams& p, int lane) {
     using Cfg = WsCfg<D>;
     constexpr int S = Cfg::kStages;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, kBlockN, false, false);
-    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, false, true);
     const WsSmem<D> sm;
     const WsGeometry g(p);
     volatile int* abort_flag = sm.abort_flag();
     const unsigned long long lim = p.wait_limit_ns;
     const uint32_t tmem = *sm.tmem_slot();
-    // S_t = Q_t·Kᵀ over D in steps of 16 (4 steps of 32 bytes per 64-wide box).
+    // S_t over D in steps of 16 (4 steps of 32 bytes per 64-wide box).
     // Descriptors advance by adding the byte offset >> 4 to the start-address field.
     auto issue_s = [&](int t, uint32_t sK) {
         const uint64_t a0 = ptx::sdesc_sw128(sm.q_tile(t), 16, 1024);
@@ -294,32 +306,9 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p, int lane) {
             ptx::mma_ss_elect(tS, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
         }
     };
-    // O_t += P_t·V over 128 keys in steps of 16 (2048 bytes of V each);
-    // V is MN-major: 64-wide swizzle atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
-    auto issue_pv_mma = [&](int t, uint32_t sV, bool accumulate) {
-        const uint64_t b0 = ptx::sdesc_sw128(sV, kBoxBytes, 1024);
-        const uint32_t tP = tmem + (t == 0 ? Cfg::kTmemP0 : Cfg::kTmemP1);
-        const uint32_t tO = tmem + (t == 0 ? Cfg::kTmemO0 : Cfg::kTmemO1);
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            ptx::mma_ts_elect(tO, tP + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
-                        (accumulate || kk > 0) ? 1u : 0u);
-        }
-    };
-    uint32_t kv_cnt = 0;
-    uint32_t p_cnt0 = 0, p_cnt1 = 0;
-    // S MMAs issued / seen consumed by the softmax, per S buffer (one shared buffer with d = 128)
+    // S MMAs issued / softmax reads seen, per S buffer (one shared buffer with d = 128)
     uint32_t s_cnt0 = 0, s_cnt1 = 0, sf_seen0 = 0, sf_seen1 = 0;
     bool ok = true;
-    // P·V of tile t. In early-S mode its completion is published on pv_done(t)
-    // for the softmax, which must not overwrite P_t or O_t before it.
-    auto issue_pv = [&](int t, uint32_t sV, bool accumulate) {
-        ptx::tc_fence_after_sync();
-        issue_pv_mma(t, sV, accumulate);
-        if (Cfg::kEarlyS) ptx::mma_commit_elect(sm.pv_done(t));
-    };
-    // S_t = Q_t·K^T once its S buffer is free: the softmax has read every
-    // earlier S written there.
     auto issue_s_safe = [&](int t, uint32_t sK) {
         const int b = Cfg::kSharedS ? 0 : t;
         uint32_t& seen = b == 0 ? sf_seen0 : sf_seen1;
@@ -335,95 +324,82 @@ __device__ __forceinline__ void ws_mma_role(const FwdParams& p, int lane) {
         ptx::mma_commit_elect(sm.s_full(t));
         return true;
     };
-    auto wait_p = [&](int t) {
-        uint32_t& c = t == 0 ? p_cnt0 : p_cnt1;
-        ok = ok && wait_phase_warp(sm.p_full(t), c & 1, abort_flag, kStatusTimeoutSoftmax, lim);
-        ++c;
-        return ok;
-    };
-    auto wait_kv = [&](uint32_t cnt) {
-        ok = ok && wait_phase_warp(sm.kv_full(cnt % S), (cnt / S) & 1, abort_flag, kStatusTimeoutLoad, lim);
-        return ok;
-    };
+    uint32_t kv_cnt = 0;
     for (int it = 0; ok; ++it) {
         const int u = next_unit(sm, it, lane, 0xffffffffu, p);
         if (u < 0) break;
         const WsItem w = item_coords<CAUSAL>(u, g);
         const int n0 = w.n0, n1 = w.n1;  // n0 <= n1 <= n0 + 1
-        const uint32_t k0 = kv_cnt;  // ring position of K_0; K_j = k0 + 2j, V_j = K_j + 1
-        auto K = [&](int j) { return k0 + 2u * j; };
-        auto V = [&](int j) { return k0 + 2u * j + 1u; };
         if (!wait_phase_warp(sm.q_full(0), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
         if (!wait_phase_warp(sm.q_full(1), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
-        if (Cfg::kSharedS) {
-            // TC order per key tile j: S0(j), PV1(j-1), S1(j), PV0(j). Each P·V
-            // of a tile precedes that tile's next S, so the commit of S_t(j)
-            // also tells the softmax that P·V_t(j-1) is done.
-            if (!(wait_kv(K(0)) && issue_s_safe(0, sm.ring(K(0))))) break;
-            if (n0 == 1) ptx::mma_commit_elect(sm.q_empty(0));
-            for (int j = 0; j < n1; ++j) {
-                if (j >= 1) {
-                    if (!(wait_kv(V(j - 1)) && wait_p(1))) break;
-                    issue_pv(1, sm.ring(V(j - 1)), j > 1);
-                    ptx::mma_commit_elect(sm.kv_empty(V(j - 1) % S));
-                }
-                if (!(wait_kv(K(j)) && issue_s_safe(1, sm.ring(K(j))))) break;
-                if (j == n1 - 1) ptx::mma_commit_elect(sm.q_empty(1));
-                ptx::mma_commit_elect(sm.kv_empty(K(j) % S));
-                if (j < n0) {
-                    if (!(wait_kv(V(j)) && wait_p(0))) break;
-                    issue_pv(0, sm.ring(V(j)), j > 0);
-                    if (j == n0 - 1) ptx::mma_commit_elect(sm.o_full(0));
-                }
-                if (j + 1 < n0) {
-                    if (!(wait_kv(K(j + 1)) && issue_s_safe(0, sm.ring(K(j + 1))))) break;
-                    if (j + 1 == n0 - 1) ptx::mma_commit_elect(sm.q_empty(0));
-                }
-            }
+        for (int j = 0; j < n1; ++j) {
+            const uint32_t k = kv_cnt + 2u * j;  // ring position of K_j
+            ok = wait_phase_warp(sm.kv_full(k % S), (k / S) & 1, abort_flag, kStatusTimeoutLoad, lim);
             if (!ok) break;
-            if (!(wait_kv(V(n1 - 1)) && wait_p(1))) break;
-            issue_pv(1, sm.ring(V(n1 - 1)), n1 > 1);
-            ptx::mma_commit_elect(sm.o_full(1));
-            ptx::mma_commit_elect(sm.kv_empty(V(n1 - 1) % S));
-        } else {
-            // early S: S_t(j) needs only K_j and the softmax's read of S_t(j-1)
-            if (!(wait_kv(K(0)) && issue_s_safe(0, sm.ring(K(0))))) break;
-            if (n0 == 1) ptx::mma_commit_elect(sm.q_empty(0));
-            if (!issue_s_safe(1, sm.ring(K(0)))) break;
-            if (n1 == 1) ptx::mma_commit_elect(sm.q_empty(1));
-            ptx::mma_commit_elect(sm.kv_empty(K(0) % S));
-            for (int j = 1; j < n1; ++j) {
-                if (!wait_kv(K(j))) break;
-                if (j < n0) {
-                    if (!issue_s_safe(0, sm.ring(K(j)))) break;
-                    if (j == n0 - 1) ptx::mma_commit_elect(sm.q_empty(0));
-                }
-                if (!issue_s_safe(1, sm.ring(K(j)))) break;
-                if (j == n1 - 1) ptx::mma_commit_elect(sm.q_empty(1));
-                ptx::mma_commit_elect(sm.kv_empty(K(j) % S));
-                if (!wait_kv(V(j - 1))) break;
-                if (j <= n0) {
-                    if (!wait_p(0)) break;
-                    issue_pv(0, sm.ring(V(j - 1)), j > 1);
-                    if (j == n0) ptx::mma_commit_elect(sm.o_full(0));
-                }
-                if (!wait_p(1)) break;
-                issue_pv(1, sm.ring(V(j - 1)), j > 1);
-                ptx::mma_commit_elect(sm.kv_empty(V(j - 1) % S));
+            if (j < n0) {
+                if (!issue_s_safe(0, sm.ring(k))) break;
+                if (j == n0 - 1) ptx::mma_commit_elect(sm.q_empty(0));
             }
-            if (!ok) break;
-            if (!wait_kv(V(n1 - 1))) break;
-            if (n0 == n1) {
-                if (!wait_p(0)) break;
-                issue_pv(0, sm.ring(V(n1 - 1)), n1 > 1);
-                ptx::mma_commit_elect(sm.o_full(0));
-            }
-            if (!wait_p(1)) break;
-            issue_pv(1, sm.ring(V(n1 - 1)), n1 > 1);
-            ptx::mma_commit_elect(sm.o_full(1));
-            ptx::mma_commit_elect(sm.kv_empty(V(n1 - 1) % S));
+            if (!issue_s_safe(1, sm.ring(k))) break;
+            if (j == n1 - 1) ptx::mma_commit_elect(sm.q_empty(1));
+            ptx::mma_commit_elect(sm.kv_empty(k % S));
         }
-        kv_cnt = k0 + 2 * n1;
+        kv_cnt += 2u * n1;
+    }
+}
+
+// O_t += P_t·V_j for tile t, once the softmax has written P_t(j); the commit
+// after each one (pv_done) tells the softmax when it may overwrite P_t or
+// rescale O_t. V slots are released by both P·V warps (two arrivals); the
+// key tiles tile 0 does not see under the causal mask are released without
+// use, after their load, so that the arrival lands in the slot's current use.
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void ws_pv_role(const FwdParams& p, int lane, int t) {
+    using Cfg = WsCfg<D>;
+    constexpr int S = Cfg::kStages;
+    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, false, true);
+    const WsSmem<D> sm;
+    const WsGeometry g(p);
+    volatile int* abort_flag = sm.abort_flag();
+    const unsigned long long lim = p.wait_limit_ns;
+    const uint32_t tmem = *sm.tmem_slot();
+    const uint32_t tP = tmem + (t == 0 ? Cfg::kTmemP0 : Cfg::kTmemP1);
+    const uint32_t tO = tmem + (t == 0 ? Cfg::kTmemO0 : Cfg::kTmemO1);
+    // 128 keys in steps of 16 (2048 bytes of V each); V is MN-major: 64-wide
+    // swizzle atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
+    auto issue_pv = [&](uint32_t sV, bool accumulate) {
+        const uint64_t b0 = ptx::sdesc_sw128(sV, kBoxBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            ptx::mma_ts_elect(tO, tP + kk * 8, b0 + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
+                              (accumulate || kk > 0) ? 1u : 0u);
+        }
+    };
+    uint32_t kv_cnt = 0, p_cnt = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+        const int u = next_unit(sm, it, lane, 0xffffffffu, p);
+        if (u < 0) break;
+        const WsItem w = item_coords<CAUSAL>(u, g);
+        const int n1 = w.n1, n_t = t == 0 ? w.n0 : w.n1;
+        for (int j = 0; j < n1; ++j) {
+            const uint32_t v = kv_cnt + 2u * j + 1u;  // ring position of V_j
+            ok = wait_phase_warp(sm.kv_full(v % S), (v / S) & 1, abort_flag, kStatusTimeoutLoad, lim);
+            if (!ok) break;
+            if (j < n_t) {
+                ok = wait_phase_warp(sm.p_full(t), p_cnt & 1, abort_flag, kStatusTimeoutSoftmax, lim);
+                ++p_cnt;
+                if (!ok) break;
+                ptx::tc_fence_after_sync();
+                issue_pv(sm.ring(v), j > 0);
+                ptx::mma_commit_elect(sm.pv_done(t));
+                if (j == n_t - 1) ptx::mma_commit_elect(sm.o_full(t));
+                ptx::mma_commit_elect(sm.kv_empty(v % S));
+            } else if (lane == 0) {
+                ptx::mbar_arrive(sm.kv_empty(v % S));
+            }
+        }
+        kv_cnt += 2u * n1;
     }
 }
 
@@ -525,7 +501,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                     s[96 + i] = __uint_as_float(r3[i]);
                 }
             }
-            // S is in registers: the MMA warp may write the next S into its buffer
+            // S is in registers: the S warp may write the next S into its buffer
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(sm.s_free(Cfg::kSharedS ? 0 : t));
@@ -547,7 +523,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                 alpha = ptx::ex2_approx(m_ref - m_tile);  // 0 on the first visible tile
                 m_ref = m_tile;
             }
-            if (Cfg::kEarlyS) {
+            {
                 // the P·V of every earlier P of this tile must be done before P and O are touched
                 bool okp = true;
                 while (okp && pv_seen < p_made) {
@@ -560,8 +536,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                 }
                 ptx::tc_fence_after_sync();
             }
-            // O_t *= alpha. (With the shared S buffer, the previous P·V of this
-            // tile was issued before S_t and finished before S_t was committed.)
+            // O_t *= alpha (every P·V into O_t so far is done).
             if (j > 0 && __any_sync(0xffffffffu, move)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 8; ++c) {
@@ -737,6 +712,8 @@ __global__ void __launch_bounds__(384, 1)
                 uint32_t count = 1;
                 if (b == sm.p_full(0) || b == sm.p_full(1) || b == sm.s_free(0) || b == sm.s_free(1))
                     count = 4;  // one arrival per softmax warp
+                for (int q = 0; q < Cfg::kStages; ++q)  // K slots (even): the S warp; V slots: both P·V warps
+                    if (b == sm.kv_empty(q)) count = (q & 1) ? 2 : 1;
                 for (int q = 0; q < Cfg::kUnitSlots; ++q)
                     if (b == sm.u_empty(q)) count = Cfg::kUnitConsumers;
                 ptx::mbar_init(b, count);
@@ -750,8 +727,19 @@ __global__ void __launch_bounds__(384, 1)
         if (warp == 9) {
             ws_load_role<D, CAUSAL>(tm_q, tm_k, tm_v, p, lane);
             __syncwarp();
-        } else if (warp == 8) {
-            ws_mma_role<D, CAUSAL>(p, lane);
+        } else {
+            // warp 8: every S; warps 10 and 11: P·V of tile 0 and tile 1
+            const int m = warp == 8 ? 0 : warp - 9;
+            if (warp == 8)
+                ws_s_role<D, CAUSAL>(p, lane);
+            else
+                ws_pv_role<D, CAUSAL>(p, lane, warp - 10);
+            __syncwarp();
+            // every MMA this warp issued is done before TMEM can be freed
+            if (lane == 0) {
+                ptx::mma_commit(sm.fin(m));
+                wait_drain(sm.fin(m), 0, 100000000ull);
+            }
             __syncwarp();
         }
         ptx::tc_fence_before_sync();
@@ -767,11 +755,6 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
         if (warp == 8) {
-            if (lane == 0) {
-                ptx::mma_commit(sm.fin());
-                wait_drain(sm.fin(), 0, 100000000ull);
-            }
-            __syncwarp();
             ptx::tc_fence_after_sync();
             ptx::tmem_dealloc(*sm.tmem_slot(), Cfg::kTmemCols);
         }
