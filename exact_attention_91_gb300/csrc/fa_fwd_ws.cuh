@@ -67,7 +67,7 @@ struct WsCfg {
     //           u_full[U] u_empty[U] pv_done[2] s_free[2]
     static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 2 + 3 + 2 * kUnitSlots + 2 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag, unit queue
-    static constexpr int kSmemBytes = kOffMisc + 8 + 4 * kUnitSlots + 8 + 1024;  // + base alignment slack
+    static constexpr int kSmemBytes = kOffMisc + 8 + 4 * kUnitSlots + 8 + 8 + 1024;  // + base alignment slack
     static constexpr int kTmemCols = 512;
     // TMEM columns. P (bf16 pairs, 64 columns per tile) never overlays S, so
     // no MMA that writes S can race a P·V that is still reading P: tcgen05.mma
@@ -116,6 +116,10 @@ struct WsSmem {
         return reinterpret_cast<volatile int*>(base + Cfg::kOffMisc + 8) + i;
     }
     // per softmax warpgroup: "this split is the last of its tile" flag
+    // per tile: how many S_t MMAs the S warp has issued so far (all units)
+    __device__ __forceinline__ volatile uint32_t* s_issued(int t) const {
+        return reinterpret_cast<volatile uint32_t*>(base + Cfg::kOffMisc + 16 + 4 * Cfg::kUnitSlots) + t;
+    }
     __device__ __forceinline__ volatile int* last_flag(int t) const {
         return reinterpret_cast<volatile int*>(base + Cfg::kOffMisc + 8 + 4 * Cfg::kUnitSlots) + t;
     }
@@ -308,6 +312,7 @@ __device__ __forceinline__ void ws_s_role(const FwdParams& p, int lane) {
     };
     // S MMAs issued / softmax reads seen, per S buffer (one shared buffer with d = 128)
     uint32_t s_cnt0 = 0, s_cnt1 = 0, sf_seen0 = 0, sf_seen1 = 0;
+    uint32_t s_iss0 = 0, s_iss1 = 0;  // S_0 / S_1 issued (differ from s_cnt with the shared buffer)
     bool ok = true;
     auto issue_s_safe = [&](int t, uint32_t sK) {
         const int b = Cfg::kSharedS ? 0 : t;
@@ -322,6 +327,9 @@ __device__ __forceinline__ void ws_s_role(const FwdParams& p, int lane) {
         issue_s(t, sK);
         ++issued;
         ptx::mma_commit_elect(sm.s_full(t));
+        uint32_t& n_iss = t == 0 ? s_iss0 : s_iss1;
+        ++n_iss;
+        if (lane == 0) *sm.s_issued(t) = n_iss;
         return true;
     };
     uint32_t kv_cnt = 0;
@@ -376,6 +384,8 @@ __device__ __forceinline__ void ws_pv_role(const FwdParams& p, int lane, int t) 
         }
     };
     uint32_t kv_cnt = 0, p_cnt = 0;
+    uint32_t s_base = 0;  // S_t MMAs of earlier units
+    volatile uint32_t* s_issued = sm.s_issued(t);
     bool ok = true;
     for (int it = 0; ok; ++it) {
         const int u = next_unit(sm, it, lane, 0xffffffffu, p);
@@ -390,6 +400,13 @@ __device__ __forceinline__ void ws_pv_role(const FwdParams& p, int lane, int t) 
                 ok = wait_phase_warp(sm.p_full(t), p_cnt & 1, abort_flag, kStatusTimeoutSoftmax, lim);
                 ++p_cnt;
                 if (!ok) break;
+                // The softmax waits for S_t(j+1) before it needs this P·V, so
+                // S_t(j+1) goes to the tensor core first: wait (briefly; this is
+                // only an ordering preference) until the S warp has issued it.
+                if (j + 1 < n_t) {
+                    const uint32_t want = s_base + static_cast<uint32_t>(j) + 2u;
+                    for (int spin = 0; spin < 2000 && *s_issued < want; ++spin) __nanosleep(32);
+                }
                 ptx::tc_fence_after_sync();
                 issue_pv(sm.ring(v), j > 0);
                 ptx::mma_commit_elect(sm.pv_done(t));
@@ -400,6 +417,7 @@ __device__ __forceinline__ void ws_pv_role(const FwdParams& p, int lane, int t) 
             }
         }
         kv_cnt += 2u * n1;
+        s_base += static_cast<uint32_t>(n_t);
     }
 }
 
@@ -719,6 +737,8 @@ __global__ void __launch_bounds__(384, 1)
                 ptx::mbar_init(b, count);
             }
             *sm.abort_flag() = 0;
+            *sm.s_issued(0) = 0u;
+            *sm.s_issued(1) = 0u;
             ptx::fence_mbar_init();
         }
         ptx::tc_fence_before_sync();
