@@ -476,7 +476,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                 break;
             }
             ptx::tc_fence_after_sync();
-            // this thread's row of S: the max of the first half overlaps the load of the second
+            // this thread's row of S, all four loads in flight at once; S is free for the next MMA once they land
             float s[kBlockN];
             float mx0, mx1, mx2, mx3;
             const int jt = w.jb + j;  // key tile index within the head
@@ -488,33 +488,16 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
                 uint32_t r0[32], r1[32], r2[32], r3[32];
                 ptx::tmem_ld_32x32b_x32(tS + 0, r0);
                 ptx::tmem_ld_32x32b_x32(tS + 32, r1);
-                ptx::tmem_wait_ld(r0);
-                ptx::reg_fence(r1);
                 ptx::tmem_ld_32x32b_x32(tS + 64, r2);
                 ptx::tmem_ld_32x32b_x32(tS + 96, r3);
+                ptx::tmem_wait_ld(r0);
+                ptx::reg_fence(r1);
+                ptx::reg_fence(r2);
+                ptx::reg_fence(r3);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     s[i] = __uint_as_float(r0[i]);
                     s[32 + i] = __uint_as_float(r1[i]);
-                }
-                if (need_mask) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = (c > last) ? -INFINITY : s[c];
-                }
-                // four independent chains of 3-input max (two new elements each),
-                // over columns 0-63 only: 64-127 are still being loaded
-                mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
-#pragma unroll
-                for (int c = 8; c < 64; c += 8) {
-                    mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
-                    mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
-                    mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
-                    mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
-                }
-                ptx::tmem_wait_ld(r2);
-                ptx::reg_fence(r3);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
                     s[64 + i] = __uint_as_float(r2[i]);
                     s[96 + i] = __uint_as_float(r3[i]);
                 }
@@ -525,10 +508,11 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
             if (lane == 0) ptx::mbar_arrive(sm.s_free(Cfg::kSharedS ? 0 : t));
             if (need_mask) {
 #pragma unroll
-                for (int c = 64; c < kBlockN; ++c) s[c] = (c > last) ? -INFINITY : s[c];
+                for (int c = 0; c < kBlockN; ++c) s[c] = (c > last) ? -INFINITY : s[c];
             }
+            mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-            for (int c = 64; c < kBlockN; c += 8) {
+            for (int c = 8; c < kBlockN; c += 8) {
                 mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
                 mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
                 mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
