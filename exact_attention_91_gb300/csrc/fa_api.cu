@@ -11,7 +11,6 @@
 #include <cuda_runtime.h>
 
 #include "fa.h"
-#include "fa_fwd_simple.cuh"
 #include "fa_fwd_ws.cuh"
 #include <cstdlib>
 
@@ -168,28 +167,6 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-template <int D, bool CAUSAL>
-int launch_simple(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                  const fa::FwdParams& prm, int dev, cudaStream_t stream) {
-    using Cfg = fa::SimpleCfg<D, true>;
-    auto kernel = fa::fa_fwd_simple_kernel<D, CAUSAL, true>;
-    const int smem = Cfg::kSmemBytes > 92 * 1024 ? Cfg::kSmemBytes : 92 * 1024;
-    static bool attr_set[kMaxDevices] = {};
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
-                cudaGetLastError();
-                return FA_ERR_LAUNCH;
-            }
-            attr_set[dev] = true;
-        }
-    }
-    const unsigned grid = static_cast<unsigned>(prm.num_q_tiles) * static_cast<unsigned>(prm.num_heads_total);
-    kernel<<<grid, Cfg::kThreads, smem, stream>>>(tq, tk, tv, to, prm);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
-}
-
 // Persistent warp-specialised kernel: one CTA per SM (its shared memory and
 // all 512 TMEM columns keep it alone on the SM), looping over work units of
 // one head x 256 query rows.
@@ -217,18 +194,9 @@ int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-bool use_simple_kernel() {
-    static const bool use_simple = [] {
-        const char* e = std::getenv("FA_KERNEL");
-        return e != nullptr && e[0] == 's';
-    }();
-    return use_simple;
-}
-
 template <int D, bool CAUSAL>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
            const fa::FwdParams& prm, int dev, int sm_count, cudaStream_t stream) {
-    if (use_simple_kernel()) return launch_simple<D, CAUSAL>(tq, tk, tv, to, prm, dev, stream);
     return launch_ws<D, CAUSAL>(tq, tk, tv, to, prm, dev, sm_count, stream);
 }
 
@@ -324,7 +292,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     const int sms = st->sm_count;
     const long long units = ((static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM)) * BH;
     const int n_k_tiles = static_cast<int>((static_cast<long long>(N) + fa::kBlockN - 1) / fa::kBlockN);
-    prm.nsplit = use_simple_kernel() ? 1 : choose_nsplit(units, n_k_tiles, sms, causal != 0);
+    prm.nsplit = choose_nsplit(units, n_k_tiles, sms, causal != 0);
     void* scratch = nullptr;
     if (prm.nsplit > 1) {
         // per call, stream-ordered: [partial O | partial LSE | tickets]
