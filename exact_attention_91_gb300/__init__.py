@@ -16,10 +16,11 @@ import os
 from .build import LIB_PATH
 
 __all__ = ["FaError", "load_library", "fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
-           "fa_set_wait_limit_ns", "fa_abi_version", "attention_forward", "EXPORTED_SYMBOLS"]
+           "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "attention_forward",
+           "EXPORTED_SYMBOLS"]
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
-                    "fa_set_wait_limit_ns", "fa_abi_version")
+                    "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout")
 
 FA_OK = 0
 FA_ERR_DEVICE_TIMEOUT = -8
@@ -56,6 +57,8 @@ def load_library(path: str | None = None):
     lib.fa_set_wait_limit_ns.restype = None
     lib.fa_abi_version.argtypes = []
     lib.fa_abi_version.restype = i
+    lib.fa_selftest_wait_timeout.argtypes = [vp, ctypes.c_ulonglong]
+    lib.fa_selftest_wait_timeout.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -95,6 +98,13 @@ def fa_set_wait_limit_ns(ns: int) -> None:
 
 def fa_abi_version() -> int:
     return load_library().fa_abi_version()
+
+
+def fa_selftest_wait_timeout(limit_ns: int, stream: int | None = None) -> int:
+    """The C ``fa_selftest_wait_timeout``: one warp waits on a barrier that
+    nothing completes until ``limit_ns`` passes, then records the timeout in
+    the device status word. Returns the launch status."""
+    return load_library().fa_selftest_wait_timeout(stream or None, limit_ns)
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,

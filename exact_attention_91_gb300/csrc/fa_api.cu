@@ -200,11 +200,36 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
     return launch_ws<D, CAUSAL>(tq, tk, tv, to, prm, dev, sm_count, stream);
 }
 
+// One warp waits on an mbarrier phase that nothing completes, through the
+// same bounded wait the forward kernel uses: after `limit_ns` it records
+// kStatusTimeoutOther in the device status word and returns.
+__global__ void __launch_bounds__(32, 1) fa_selftest_timeout_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        fa::ptx::mbar_init(fa::ptx::smem_u32(&bar), 1);
+        fa::ptx::fence_mbar_init();
+    }
+    __syncwarp();
+    fa::wait_phase_warp(fa::ptx::smem_u32(&bar), 0, &abort_flag, fa::kStatusTimeoutOther, limit_ns);
+}
+
 }  // namespace
 
 extern "C" {
 
 int fa_abi_version(void) { return FA_ABI_VERSION; }
+
+int fa_selftest_wait_timeout(void* stream, unsigned long long limit_ns) {
+    int dev = -1;
+    DeviceState* st = nullptr;
+    const int rc = probe_device(&dev, &st);
+    if (rc != FA_OK) return rc;
+    if (limit_ns < 200000ull || limit_ns > 1000000000ull) return FA_ERR_BAD_SHAPE;
+    fa_selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
 
 const char* fa_strerror(int status) {
     switch (status) {

@@ -121,6 +121,19 @@ int fa_device_status(void* stream, unsigned* bits);
  */
 void fa_set_wait_limit_ns(unsigned long long ns);
 
+/*
+ * fa_selftest_wait_timeout — failure-detection self-test. Launches, on
+ * `stream`, one warp that waits on an mbarrier phase nothing completes, using
+ * the forward kernel's bounded wait with a limit of `limit_ns` (200 µs to 1 s,
+ * else FA_ERR_BAD_SHAPE). The wait gives up, records "other wait" (bit 4) in
+ * the device status word and the kernel returns; nothing faults or hangs, and
+ * the context stays usable. fa_device_status() then reports
+ * FA_ERR_DEVICE_TIMEOUT. Returns FA_OK once launched, FA_ERR_NO_DEVICE /
+ * FA_ERR_UNSUPPORTED_ARCH / FA_ERR_LAUNCH otherwise. The pages have no
+ * counterpart (they have no failure handling).
+ */
+int fa_selftest_wait_timeout(void* stream, unsigned long long limit_ns);
+
 /* ABI version of this header (bumped on any incompatible change). */
 int fa_abi_version(void);
 

@@ -74,6 +74,7 @@ def test_valid_call_without_gpu_reports_no_device(lib):
         pytest.skip("a GPU is present")
     assert _call() == -5
     assert _call(lse=0) == -5
+    assert lib.fa_selftest_wait_timeout(None, 1_000_000) == -5
 
 
 def test_missing_library_fails_loudly(tmp_path):
