@@ -68,10 +68,11 @@ def _load():
     lib.oracle_attn_rows_f64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, D, I, lp, L, I]
     lib.oracle_attn_online_f64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, D, I, L, I]
     lib.oracle_attn_probs_f64.argtypes = [dp, dp, dp, L, L, D, I]
+    lib.oracle_attn_varlen_f64.argtypes = [dp, dp, dp, dp, dp, lp, lp, L, L, L, D, I, I]
     lib.oracle_host_threads.argtypes = []
     for fn in (lib.oracle_attn_fwd_f64, lib.oracle_attn_rows_f64,
                lib.oracle_attn_online_f64, lib.oracle_attn_probs_f64,
-               lib.oracle_host_threads):
+               lib.oracle_attn_varlen_f64, lib.oracle_host_threads):
         fn.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -153,3 +154,28 @@ def attn_probs(q, k, scale: float, causal: bool):
 
 if __name__ == "__main__":  # pragma: no cover - manual build helper
     print(build(force="--force" in sys.argv))
+
+
+def attn_varlen(q, k, v, cu_q, cu_k, scale: float, causal: bool, nthreads: int = 0):
+    """Variable-length batch by the definition: q [total_q, H, d], k and v
+    [total_k, H, d], sequence b = query tokens cu_q[b]:cu_q[b+1] and key
+    tokens cu_k[b]:cu_k[b+1]; the causal mask aligns each sequence's last
+    query with its last key. Returns O [total_q, H, d] and LSE [H, total_q]
+    (fp64); a query that sees no key gives O = 0 and LSE = -inf."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 3 or k.ndim != 3 or v.shape != k.shape or q.shape[1:] != k.shape[1:]:
+        raise ValueError("expected q [total_q, H, d], k and v [total_k, H, d]")
+    cu_q = np.ascontiguousarray(cu_q, dtype=np.int64)
+    cu_k = np.ascontiguousarray(cu_k, dtype=np.int64)
+    B = cu_q.shape[0] - 1
+    if cu_k.shape[0] != B + 1 or cu_q[-1] != q.shape[0] or cu_k[-1] != k.shape[0]:
+        raise ValueError("cu_seqlens do not match the token counts")
+    H, d = q.shape[1], q.shape[2]
+    o = np.empty(q.shape, np.float64)
+    lse = np.empty((H, q.shape[0]), np.float64)
+    lp = ctypes.POINTER(ctypes.c_long)
+    _check(_load().oracle_attn_varlen_f64(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), cu_q.ctypes.data_as(lp),
+        cu_k.ctypes.data_as(lp), B, H, d, float(scale), int(bool(causal)), int(nthreads)),
+        "attn_varlen")
+    return o, lse

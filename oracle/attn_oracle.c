@@ -31,6 +31,12 @@
  * claim the method rests on ("Mini FlashAttention", §4; "How Did I Write My
  * First FlashAttention Kernel in CUDA?", the surrogate-output paragraph).
  *
+ * A third entry point takes a variable-length batch: sequences with their
+ * own query and key counts, tokens stored as rows of [total, H, d], and the
+ * causal mask aligned so that each sequence's last query sees its last key
+ * (the plainest reading for queries and keys of different lengths; with equal
+ * lengths it is the mask above). It calls the same per-row definition.
+ *
  * Every function returns 0 on success and a negative value on bad arguments.
  * Threads (POSIX) split independent query rows; each row is computed by one
  * thread in a fixed order, so results do not depend on the thread count.
@@ -44,9 +50,10 @@
 /* ---------- one query row, by the definition ------------------------------ */
 
 /* Row i of head (q_row, k, v): keys 0 .. n_keys-1 take part (n_keys = N, or
- * i+1 under the causal mask). s_buf holds n_keys doubles of scratch. */
+ * i+1 under the causal mask). Key j's row of K and V starts at j * kv_stride.
+ * s_buf holds n_keys doubles of scratch. */
 static void definition_row(const double *q_row, const double *k, const double *v,
-                           long n_keys, long d, double scale, double *s_buf,
+                           long n_keys, long d, long kv_stride, double scale, double *s_buf,
                            double *o_row, double *lse_out)
 {
     long j, c;
@@ -58,7 +65,7 @@ static void definition_row(const double *q_row, const double *k, const double *v
     /* S[i, j] = scale * <Q[i], K[j]> */
     for (j = 0; j < n_keys; ++j) {
         double x = 0.0;
-        for (c = 0; c < d; ++c) x += q_row[c] * k[j * d + c];
+        for (c = 0; c < d; ++c) x += q_row[c] * k[j * kv_stride + c];
         s_buf[j] = scale * x;
     }
     /* P[i, :] = softmax(S[i, :]): max, sum of exponentials, normalise */
@@ -71,7 +78,7 @@ static void definition_row(const double *q_row, const double *k, const double *v
     for (c = 0; c < d; ++c) o_row[c] = 0.0;
     for (j = 0; j < n_keys; ++j) {
         const double p = s_buf[j];
-        for (c = 0; c < d; ++c) o_row[c] += p * v[j * d + c];
+        for (c = 0; c < d; ++c) o_row[c] += p * v[j * kv_stride + c];
     }
     *lse_out = m + log(z);
 }
@@ -168,7 +175,7 @@ static void *worker(void *arg)
             if (job->chunk > 0)
                 online_row(q_row, k, v, n_keys, d, job->scale, job->chunk, s_buf, acc, o_row, lse);
             else
-                definition_row(q_row, k, v, n_keys, d, job->scale, s_buf, o_row, lse);
+                definition_row(q_row, k, v, n_keys, d, d, job->scale, s_buf, o_row, lse);
         }
     }
     free(s_buf);
@@ -206,6 +213,69 @@ static int run_job(job_t *job, int nthreads)
 static int check_shape(long B, long H, long N, long d)
 {
     return (B < 0 || H < 0 || N < 0 || d <= 0) ? -2 : 0;
+}
+
+/* ---------- variable-length batches -------------------------------------- */
+
+/* Sequence b holds query tokens cu_q[b] .. cu_q[b+1]-1 and key tokens
+ * cu_k[b] .. cu_k[b+1]-1 (Nq and Nk of them). Tokens are rows of [total, H, d]
+ * (a token's H heads side by side). Under the causal mask the last query of a
+ * sequence lines up with its last key: query i (0-based in its sequence) sees
+ * keys j <= i + Nk - Nq, a prefix of the sequence's keys; a query that sees
+ * none gives O = 0 and LSE = -inf. Rows are numbered h * total_q + token,
+ * which is also the LSE layout [H, total_q]. */
+typedef struct {
+    const double *q, *k, *v;
+    double *o, *lse;
+    const long *cu_q, *cu_k;
+    long B, H, d, total_q;
+    double scale;
+    int causal;
+    long max_nk;
+    long next;
+    pthread_mutex_t lock;
+    int failed;
+} vjob_t;
+
+static void *varlen_worker(void *arg)
+{
+    vjob_t *job = (vjob_t *)arg;
+    const long H = job->H, d = job->d, n_rows = job->H * job->total_q;
+    double *s_buf = (double *)malloc(sizeof(double) * (size_t)(job->max_nk > 0 ? job->max_nk : 1));
+    if (!s_buf) {
+        pthread_mutex_lock(&job->lock);
+        job->failed = 1;
+        pthread_mutex_unlock(&job->lock);
+        return NULL;
+    }
+    for (;;) {
+        pthread_mutex_lock(&job->lock);
+        long start = job->next;
+        job->next += ROWS_PER_GRAB;
+        pthread_mutex_unlock(&job->lock);
+        if (start >= n_rows) break;
+        long stop = start + ROWS_PER_GRAB < n_rows ? start + ROWS_PER_GRAB : n_rows;
+        for (long r = start; r < stop; ++r) {
+            long h = r / job->total_q, tok = r % job->total_q;
+            long b = 0; /* the sequence holding query token tok */
+            while (b + 1 < job->B && job->cu_q[b + 1] <= tok) ++b;
+            long nq = job->cu_q[b + 1] - job->cu_q[b], nk = job->cu_k[b + 1] - job->cu_k[b];
+            long i = tok - job->cu_q[b];
+            long n_keys = nk;
+            if (job->causal) {
+                n_keys = i + nk - nq + 1;
+                if (n_keys < 0) n_keys = 0;
+                if (n_keys > nk) n_keys = nk;
+            }
+            const double *q_row = job->q + (tok * H + h) * d;
+            const double *k = job->k + (job->cu_k[b] * H + h) * d;
+            const double *v = job->v + (job->cu_k[b] * H + h) * d;
+            definition_row(q_row, k, v, n_keys, d, H * d, job->scale, s_buf,
+                           job->o + (tok * H + h) * d, job->lse + r);
+        }
+    }
+    free(s_buf);
+    return NULL;
 }
 
 /* ---------- exported entry points ----------------------------------------- */
@@ -273,4 +343,43 @@ int oracle_attn_probs_f64(const double *q, const double *k, double *p,
         for (long j = 0; j < n_keys; ++j) row[j] = exp(row[j] - m) / z;
     }
     return 0;
+}
+
+/* Variable-length batch by the definition. q, o: [total_q, H, d]; k, v:
+ * [total_k, H, d]; lse: [H, total_q]; cu_q, cu_k: B+1 non-decreasing offsets
+ * from 0 (total_q = cu_q[B], total_k = cu_k[B]). */
+int oracle_attn_varlen_f64(const double *q, const double *k, const double *v,
+                           double *o, double *lse, const long *cu_q, const long *cu_k,
+                           long B, long H, long d, double scale, int causal, int nthreads)
+{
+    if (!q || !k || !v || !o || !lse || !cu_q || !cu_k) return -1;
+    if (B < 1 || H < 1 || d <= 0 || cu_q[0] != 0 || cu_k[0] != 0) return -2;
+    long max_nk = 0;
+    for (long b = 0; b < B; ++b) {
+        if (cu_q[b + 1] < cu_q[b] || cu_k[b + 1] < cu_k[b]) return -2;
+        if (cu_k[b + 1] - cu_k[b] > max_nk) max_nk = cu_k[b + 1] - cu_k[b];
+    }
+    vjob_t job;
+    memset(&job, 0, sizeof(job));
+    job.q = q; job.k = k; job.v = v; job.o = o; job.lse = lse;
+    job.cu_q = cu_q; job.cu_k = cu_k;
+    job.B = B; job.H = H; job.d = d; job.total_q = cu_q[B];
+    job.scale = scale; job.causal = causal; job.max_nk = max_nk;
+    long n_rows = H * job.total_q;
+    if (n_rows == 0) return 0;
+    long n = nthreads > 0 ? nthreads : host_threads();
+    if (n > n_rows) n = n_rows;
+    pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n);
+    if (!tids) return -3;
+    pthread_mutex_init(&job.lock, NULL);
+    long started = 0;
+    for (long t = 0; t < n; ++t) {
+        if (pthread_create(&tids[t], NULL, varlen_worker, &job) != 0) break;
+        ++started;
+    }
+    if (started == 0) varlen_worker(&job);
+    for (long t = 0; t < started; ++t) pthread_join(tids[t], NULL);
+    pthread_mutex_destroy(&job.lock);
+    free(tids);
+    return job.failed ? -3 : 0;
 }
