@@ -16,10 +16,10 @@ import os
 from .build import LIB_PATH
 
 __all__ = ["FaError", "load_library", "fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
-           "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "attention_forward",
-           "EXPORTED_SYMBOLS"]
+           "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_fwd_varlen",
+           "attention_forward", "attention_forward_varlen", "EXPORTED_SYMBOLS"]
 
-EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_noalloc", "fa_fwd_varlen", "fa_strerror", "fa_device_status",
                     "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout")
 
 FA_OK = 0
@@ -49,6 +49,8 @@ def load_library(path: str | None = None):
     lib.fa_fwd.restype = i
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd_noalloc.restype = i
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_varlen.restype = i
     lib.fa_strerror.argtypes = [i]
     lib.fa_strerror.restype = ctypes.c_char_p
     lib.fa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -79,6 +81,14 @@ def fa_fwd_noalloc(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: i
     must not be issued. Returns the status code."""
     return load_library().fa_fwd_noalloc(q, k, v, o, lse or None, B, H, N, d, scale, int(bool(causal)),
                                          stream or None)
+
+
+def fa_fwd_varlen(q: int, k: int, v: int, o: int, lse: int | None, cu_q: int, cu_k: int, B: int, H: int,
+                  total_q: int, total_k: int, max_seqlen_q: int, d: int, scale: float, causal: bool,
+                  stream: int | None) -> int:
+    """The C ``fa_fwd_varlen``: device pointers as ints, returns the status code."""
+    return load_library().fa_fwd_varlen(q, k, v, o, lse or None, cu_q, cu_k, B, H, total_q, total_k,
+                                        max_seqlen_q, d, scale, int(bool(causal)), stream or None)
 
 
 def fa_strerror(status: int) -> str:
@@ -136,4 +146,43 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
                 s.cuda_stream)
     if rc != FA_OK:
         raise FaError(rc)
+    return (out, lse) if return_lse else out
+
+
+def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool = False,
+                             scale: float | None = None, out=None, lse=None, return_lse: bool = True,
+                             stream=None):
+    """O [total_q, H, d] (bf16) and LSE [H, total_q] (fp32) for a batch of
+    sequences of different lengths: q [total_q, H, d], k and v [total_k, H, d]
+    (bf16, CUDA, contiguous), int32 CUDA offsets ``cu_seqlens_q`` /
+    ``cu_seqlens_k`` of B + 1 entries. Under ``causal`` each sequence's last
+    query is aligned with its last key."""
+    import torch
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k, v must be bf16")
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or q.shape[1:] != k.shape[1:]:
+        raise ValueError("q must be [total_q, H, d] and k, v [total_k, H, d]")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_k.shape != cu_seqlens_q.shape or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 offsets")
+    for t in (q, k, v, cu_seqlens_q, cu_seqlens_k):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all inputs must be contiguous CUDA tensors")
+    total_q, H, d = q.shape
+    total_k = k.shape[0]
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       lse.data_ptr() if lse is not None else None, cu_seqlens_q.data_ptr(),
+                       cu_seqlens_k.data_ptr(), B, H, total_q, total_k, int(max_seqlen_q), d, float(scale),
+                       causal, s.cuda_stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_varlen")
     return (out, lse) if return_lse else out

@@ -12,6 +12,7 @@
 
 #include "fa.h"
 #include "fa_fwd_ws.cuh"
+#include "fa_fwd_varlen.cuh"
 #include <cstdlib>
 
 namespace {
@@ -162,6 +163,21 @@ int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// 3-D view (d, H, total) of a token-major bf16 [total, H, d] tensor: a box is
+// 128 consecutive tokens x 64 columns of one head. Tokens past `total` read
+// as zero.
+int encode_map_tokens(CUtensorMap* map, const void* ptr, int total, int H, int d) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(total)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(fa::kBoxCols), 1, static_cast<cuuint32_t>(fa::kBlockM)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_LAUNCH;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + nb && y < x + na;
@@ -213,6 +229,32 @@ __global__ void __launch_bounds__(32, 1) fa_selftest_timeout_kernel(unsigned lon
     }
     __syncwarp();
     fa::wait_phase_warp(fa::ptx::smem_u32(&bar), 0, &abort_flag, fa::kStatusTimeoutOther, limit_ns);
+}
+
+// The variable-length kernel: same launch shape, one unit per (sequence,
+// head, 256-query block) of the longest sequence.
+template <int D, bool CAUSAL>
+int launch_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const fa::vl::VlParams& prm, int dev, int sm_count, cudaStream_t stream) {
+    using Cfg = fa::WsCfg<D>;
+    auto kernel = fa::vl::fa_fwd_varlen_kernel<D, CAUSAL>;
+    static bool attr_set[kMaxDevices] = {};
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return FA_ERR_LAUNCH;
+            }
+            attr_set[dev] = true;
+        }
+    }
+    const long long nqb = (static_cast<long long>(prm.max_nq) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+    const long long items = nqb * prm.num_heads_total;
+    const unsigned grid = static_cast<unsigned>(items < sm_count ? items : sm_count);
+    kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -349,6 +391,72 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         if (rc == FA_OK) rc = FA_ERR_LAUNCH;
     }
     return rc;
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int B, int H, int total_q, int total_k, int max_seqlen_q, int d,
+                  float scale, int causal, void* stream) {
+    if (B < 1 || H < 1 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_q > total_q)
+        return FA_ERR_BAD_SHAPE;
+    // (an empty tensor may come with a null pointer)
+    if (!cu_seqlens_q || !cu_seqlens_k || (total_q > 0 && (!q || !o)) || (total_k > 0 && (!k || !v)))
+        return FA_ERR_NULL_PTR;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEAD_DIM;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long nqb = (static_cast<long long>(max_seqlen_q) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+    if (BH > 0x7fffffffLL || BH * nqb > 0x7fffffffLL ||
+        static_cast<long long>(total_q) * H * d > 0x7fffffffLL || static_cast<long long>(total_k) * H * d > 0x7fffffffLL)
+        return FA_ERR_BAD_SHAPE;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||
+        ((reinterpret_cast<uintptr_t>(cu_seqlens_q) | reinterpret_cast<uintptr_t>(cu_seqlens_k)) & 3u) != 0)
+        return FA_ERR_MISALIGNED;
+    const size_t q_bytes = static_cast<size_t>(total_q) * H * d * 2, k_bytes = static_cast<size_t>(total_k) * H * d * 2;
+    const size_t lse_bytes = static_cast<size_t>(total_q) * H * 4;
+    if (overlaps(o, q_bytes, q, q_bytes) || overlaps(o, q_bytes, k, k_bytes) || overlaps(o, q_bytes, v, k_bytes))
+        return FA_ERR_ALIAS;
+    if (lse && (overlaps(lse, lse_bytes, q, q_bytes) || overlaps(lse, lse_bytes, k, k_bytes) ||
+                overlaps(lse, lse_bytes, v, k_bytes) || overlaps(lse, lse_bytes, o, q_bytes)))
+        return FA_ERR_ALIAS;
+
+    int dev = -1;
+    DeviceState* st = nullptr;
+    int rc = probe_device(&dev, &st);
+    if (rc != FA_OK) return rc;
+    if (total_q == 0 || max_seqlen_q == 0) return FA_OK;  // no query: nothing to write
+
+    CUtensorMap tq, tk, tv;
+    // a map needs at least one row: an empty key set is read through a one-row view of q
+    if (encode_map_tokens(&tq, q, total_q, H, d) != FA_OK ||
+        encode_map_tokens(&tk, total_k ? k : q, total_k ? total_k : 1, H, d) != FA_OK ||
+        encode_map_tokens(&tv, total_k ? v : q, total_k ? total_k : 1, H, d) != FA_OK)
+        return FA_ERR_LAUNCH;
+
+    fa::vl::VlParams prm{};
+    prm.o = o;
+    prm.lse = lse;
+    prm.cu_q = cu_seqlens_q;
+    prm.cu_k = cu_seqlens_k;
+    prm.heads = H;
+    prm.num_heads_total = static_cast<int>(BH);
+    prm.total_q = total_q;
+    prm.max_nq = max_seqlen_q;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        prm.wait_limit_ns = g_wait_limit_ns;
+    }
+    if (ensure_sched(*st) != FA_OK) return FA_ERR_LAUNCH;
+    prm.sched = st->sched + (st->sched_next.fetch_add(1) % kSchedSlots) * kSchedSlotWords;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int sms = st->sm_count;
+    if (d == 64)
+        return causal ? launch_varlen<64, true>(tq, tk, tv, prm, dev, sms, s)
+                      : launch_varlen<64, false>(tq, tk, tv, prm, dev, sms, s);
+    return causal ? launch_varlen<128, true>(tq, tk, tv, prm, dev, sms, s)
+                  : launch_varlen<128, false>(tq, tk, tv, prm, dev, sms, s);
 }
 
 }  // extern "C"

@@ -144,3 +144,31 @@ def make_inputs(w: Workload) -> Inputs:
         q = bf16_from_f64(q64)
         return Inputs(w, q, k, v, spike)
     raise ValueError(f"unknown value recipe {w.values!r}")
+
+
+@dataclasses.dataclass
+class VarlenInputs:
+    seqlens_q: tuple
+    seqlens_k: tuple
+    cu_q: np.ndarray         # int32 [B + 1]
+    cu_k: np.ndarray
+    q: np.ndarray            # uint16 bf16 bits [total_q, H, d]
+    k: np.ndarray            # [total_k, H, d]
+    v: np.ndarray
+
+    def f64(self):
+        return bf16_to_f64(self.q), bf16_to_f64(self.k), bf16_to_f64(self.v)
+
+
+def make_varlen_inputs(seqlens_q, seqlens_k, H: int, d: int, seed: int) -> VarlenInputs:
+    """A batch of sequences of their own query and key counts, token-major
+    [total, H, d] bf16 with Q, K, V iid N(0, 1), and the int32 offsets."""
+    if len(seqlens_q) != len(seqlens_k) or len(seqlens_q) < 1:
+        raise ValueError("one query count and one key count per sequence")
+    cu_q = np.concatenate([[0], np.cumsum(seqlens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(seqlens_k)]).astype(np.int32)
+    gq, gk, gv = [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(3)]
+    q = bf16_from_f64(gq.standard_normal((int(cu_q[-1]), H, d)))
+    k = bf16_from_f64(gk.standard_normal((int(cu_k[-1]), H, d)))
+    v = bf16_from_f64(gv.standard_normal((int(cu_k[-1]), H, d)))
+    return VarlenInputs(tuple(seqlens_q), tuple(seqlens_k), cu_q, cu_k, q, k, v)

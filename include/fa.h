@@ -101,6 +101,41 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int H, int N, int d, float scale, int causal, void* stream);
 
+/*
+ * fa_fwd_varlen — the same forward pass over a batch of B sequences of
+ * different lengths, each with its own number of queries and keys ("Mini
+ * FlashAttention", §4 "The flash trick: online softmax", checks the loop on
+ * ragged sequences).
+ *
+ *   q, o   bf16 [total_q, H, d], token-major (a token's H heads side by side),
+ *          device, contiguous, 16-byte aligned
+ *   k, v   bf16 [total_k, H, d], likewise
+ *   lse    fp32 [H, total_q], device, or NULL; natural-log log-sum-exp
+ *   cu_seqlens_q, cu_seqlens_k
+ *          int32 [B + 1], device: sequence b holds query tokens
+ *          cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key tokens
+ *          cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1. The caller guarantees
+ *          cu[0] = 0, non-decreasing offsets, cu_seqlens_q[B] = total_q,
+ *          cu_seqlens_k[B] = total_k and every query count <= max_seqlen_q;
+ *          the library reads them only on the GPU. Offsets that break this
+ *          give undefined values but no write outside o[0, total_q) and
+ *          lse's rows (reads past total_k see zeros).
+ *   max_seqlen_q
+ *          the largest query count of the batch (it sizes the launch)
+ *   causal non-zero: the mask is aligned at the end of each sequence, so
+ *          query i (0-based within its sequence) sees keys j <= i + Nk - Nq;
+ *          with Nq = Nk this is fa_fwd's mask, and a single query (decode)
+ *          sees every key. A query that sees no key gets O = 0, LSE = -inf.
+ *
+ * Same return codes as fa_fwd (FA_ERR_BAD_SHAPE also for negative totals or
+ * max_seqlen_q > total_q; q/o and k/v may be NULL when total_q, resp.
+ * total_k, is 0); a batch with no query returns FA_OK at once. The
+ * key range of a unit is never split (no scratch memory is used).
+ */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H, int total_q,
+                  int total_k, int max_seqlen_q, int d, float scale, int causal, void* stream);
+
 /* Static English text for a return code (never NULL). */
 const char* fa_strerror(int status);
 

@@ -80,3 +80,18 @@ def test_valid_call_without_gpu_reports_no_device(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(FileNotFoundError):
         fa.load_library(str(tmp_path / "libfa.so"))
+
+
+def test_varlen_bad_arguments_are_rejected_before_launch(lib):
+    """fa_fwd_varlen validates on the host before it looks for a device."""
+    p = 1 << 20  # aligned stand-in pointers; nothing is dereferenced on these paths
+    f = lib.fa_fwd_varlen
+    #          q  k  v  o        lse   cu_q  cu_k  B  H  tq tk  mq  d    scale causal stream
+    assert f(p, p, p, p + 4096, None, p, p, 0, 2, 8, 8, 8, 64, 0.125, 0, None) == -2   # B < 1
+    assert f(p, p, p, p + 4096, None, p, p, 1, 2, 8, 8, 9, 64, 0.125, 0, None) == -2   # max_seqlen_q > total_q
+    assert f(p, p, p, p + 4096, None, None, p, 1, 2, 8, 8, 8, 64, 0.125, 0, None) == -1
+    assert f(None, p, p, p + 4096, None, p, p, 1, 2, 8, 8, 8, 64, 0.125, 0, None) == -1
+    assert f(p, p, p, p + 4096, None, p, p, 1, 2, 8, 8, 8, 96, 0.125, 0, None) == -3
+    assert f(p, p, p, p + 4096, None, p, p, 1, 2, 8, 8, 8, 64, 0.0, 0, None) == -9
+    assert f(p + 2, p, p, p + 4096, None, p, p, 1, 2, 8, 8, 8, 64, 0.125, 0, None) == -4
+    assert f(p, p, p, p + 64, None, p, p, 1, 2, 8, 8, 8, 64, 0.125, 0, None) == -10  # o overlaps q
