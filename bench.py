@@ -438,6 +438,105 @@ def run_ours(args, w: fin.Workload):
     return 0
 
 
+# Variable-length batches (fa_fwd_varlen), measured apart from the headline:
+#   prefill_mix  16 sequences with lengths drawn from U{256..8192} (Nq = Nk),
+#                H = 32, d = 128, causal: tensor-bound, TFLOP/s counted like
+#                the dense metric (4·H·d·N²/2 per causal sequence)
+#   decode       64 sequences of one query against 8192 keys, H = 32,
+#                d = 128, causal (the last query sees every key): bound by
+#                reading K and V, reported as GB/s of compulsory bytes
+VARLEN_MIXES = ("prefill_mix", "decode")
+
+
+def varlen_batch(name: str):
+    g = np.random.Generator(np.random.PCG64(fin.SEED_BASE + 70))
+    if name == "prefill_mix":
+        n = [int(x) for x in g.integers(256, 8193, size=16)]
+        return n, n, 32, 128, True
+    return [1] * 64, [8192] * 64, 32, 128, True
+
+
+def run_varlen(args) -> int:
+    import torch
+    import exact_attention_91_gb300 as fa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    sq, sk, H, d, causal = varlen_batch(args.varlen)
+    x = fin.make_varlen_inputs(sq, sk, H, d, seed=fin.SEED_BASE + 71)
+    up = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    q, k, v = up(x.q), up(x.k), up(x.v)
+    cu_q, cu_k = torch.from_numpy(x.cu_q).to(dev), torch.from_numpy(x.cu_k).to(dev)
+    total_q, total_k = q.shape[0], k.shape[0]
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total_q), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(d)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    def launch():
+        rc = fa.fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              cu_q.data_ptr(), cu_k.data_ptr(), len(sq), H, total_q, total_k, max(sq), d,
+                              scale, causal, sp)
+        if rc != 0:
+            raise fa.FaError(rc, "fa_fwd_varlen")
+
+    bytes_step = (2 * total_q + 2 * total_k) * H * d * 2 + total_q * H * 4
+    flops_step = sum(4.0 * H * d * (nq * nk / 2 if causal and nq == nk else
+                                    (nq * nk if not causal else sum(min(nk, i + nk - nq + 1) for i in range(nq))))
+                     for nq, nk in zip(sq, sk))
+    flush = None if bytes_step > 2 * L2_BYTES else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(None)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 0)):
+            launch()
+            if flush is not None:
+                flush.zero_()
+    stream.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+            if flush is not None:
+                flush.zero_()
+    stream.synchronize()
+    wall1 = time.time()
+    sampler.stop()
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / args.steps
+    peaks = load_peaks() or {}
+    if args.varlen == "decode":
+        value, unit = bytes_step / (ms * 1e-3) / 1e9, "GB/s"
+        peak = float(peaks.get("hbm_gbs", 6800.0))
+        roof = {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                "traffic": None, "bytes_per_launch": bytes_step}
+        metric = "variable-length attention fwd (decode) GB/s of compulsory bytes at 1 GPU"
+    else:
+        value, unit = flops_step / (ms * 1e-3) / 1e12, "TFLOP/s"
+        peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+        roof = {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
+                "traffic": None, "flops_per_launch": flops_step}
+        metric = "variable-length attention fwd TFLOP/s at 1 GPU"
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"varlen_{args.varlen}", "B": len(sq), "H": H, "d": d, "causal": causal,
+                   "seqlens_q": sq if len(set(sq)) > 1 else f"{len(sq)} x {sq[0]}",
+                   "seqlens_k": sk if len(set(sk)) > 1 else f"{len(sk)} x {sk[0]}",
+                   "l2": "inputs larger than L2" if flush is None else "L2 flushed between timed launches"},
+        "roofline": roof, "gpu_launches": args.steps, "clocks": sampler.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -448,6 +547,8 @@ def main(argv=None):
     ap.add_argument("--shape", default=None,
                     help="B,H,N,d,causal: a custom shape with N(0,1) values instead of a named workload "
                          "(for profiling small cases)")
+    ap.add_argument("--varlen", choices=VARLEN_MIXES, default=None,
+                    help="measure fa_fwd_varlen on a synthetic variable-length batch instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
@@ -457,6 +558,8 @@ def main(argv=None):
     if args.shape:
         B, H, N, d, causal = (int(x) for x in args.shape.split(","))
         w = fin.custom(B, H, N, d, bool(causal), seed=fin.SEED_BASE + 99)
+    if args.varlen:
+        return run_varlen(args)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -405,9 +405,8 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
     const long long BH = static_cast<long long>(B) * H;
     const long long nqb = (static_cast<long long>(max_seqlen_q) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-    if (BH > 0x7fffffffLL || BH * nqb > 0x7fffffffLL ||
-        static_cast<long long>(total_q) * H * d > 0x7fffffffLL || static_cast<long long>(total_k) * H * d > 0x7fffffffLL)
-        return FA_ERR_BAD_SHAPE;
+    // (element offsets are 64-bit; token indices and the unit count must fit in int)
+    if (BH > 0x7fffffffLL || BH * nqb > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
     if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||

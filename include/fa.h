@@ -127,9 +127,10 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
  *          with Nq = Nk this is fa_fwd's mask, and a single query (decode)
  *          sees every key. A query that sees no key gets O = 0, LSE = -inf.
  *
- * Same return codes as fa_fwd (FA_ERR_BAD_SHAPE also for negative totals or
- * max_seqlen_q > total_q; q/o and k/v may be NULL when total_q, resp.
- * total_k, is 0); a batch with no query returns FA_OK at once. The
+ * Same return codes as fa_fwd (FA_ERR_BAD_SHAPE for negative totals,
+ * max_seqlen_q > total_q, or B*H*ceil(max_seqlen_q/256) >= 2^31; q/o and k/v
+ * may be NULL when total_q, resp. total_k, is 0); a batch with no query
+ * returns FA_OK at once. The
  * key range of a unit is never split (no scratch memory is used).
  */
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
