@@ -161,6 +161,30 @@ def dist_env():
     return world, rank, local
 
 
+def rank_workload(w: fin.Workload, rank: int, world: int) -> fin.Workload:
+    """Each rank's own batch: the same shape, independently seeded (weak
+    scaling: heads are independent, so ranks share nothing)."""
+    if world == 1:
+        return w
+    return fin.Workload(w.name, w.B, w.H, w.N, w.d, w.causal, w.values, w.seed + 1000 * rank)
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (every rank must call it)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, flops_step: float, ms_total: float) -> float:
+    """Whole-job TFLOP/s: every rank's steps over the slowest rank's time."""
+    return world * steps * flops_step / (ms_total * 1e-3) / 1e12
+
+
 def cpu_model() -> str:
     try:
         with open("/proc/cpuinfo", encoding="utf-8") as f:
@@ -283,9 +307,7 @@ def run_ours(args, w: fin.Workload):
     dev = torch.device("cuda", local)
     fa.load_library()
 
-    wr = w if world == 1 else fin.Workload(w.name, w.B, w.H, w.N, w.d, w.causal, w.values,
-                                           w.seed + 1000 * rank)
-    x = fin.make_inputs(wr)
+    x = fin.make_inputs(rank_workload(w, rank, world))
 
     def up(a):
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -351,12 +373,7 @@ def run_ours(args, w: fin.Workload):
     kernel_ms = sum(launch_ms)
     region_ms = t_begin.elapsed_time(t_end)
     # with an L2 flush between launches the flush is not part of the work
-    step_total_ms = kernel_ms if flush is not None else region_ms
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([step_total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_total_ms = float(t.item())
+    step_total_ms = max_over_ranks(kernel_ms if flush is not None else region_ms, world, dev)
     clocks = sampler.summary(wall0, wall1)
 
     # ---- end to end: pinned host buffers, copies inside the timed region
@@ -386,17 +403,12 @@ def run_ours(args, w: fin.Workload):
             e2e_step()
         e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     sampler.stop()
 
     flops_step = w.flops
-    value = world * args.steps * flops_step / (step_total_ms * 1e-3) / 1e12
-    e2e_value = world * e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
+    value = job_throughput(world, args.steps, flops_step, step_total_ms)
+    e2e_value = job_throughput(world, e2e_steps, flops_step, e2e_ms)
     avg_launch_s = kernel_ms / args.steps * 1e-3
     achieved = flops_step / avg_launch_s / 1e12
     peaks = load_peaks()

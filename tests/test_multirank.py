@@ -1,0 +1,69 @@
+"""The bench's multi-rank host logic on CPU, with two gloo ranks: every rank
+runs its own independently seeded batch (no data-path collective), the time
+reported is the slowest rank's, and the throughput counts every rank's work.
+The reference arm runs on rank 0 only."""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import bench  # noqa: E402
+from exact_attention_91_gb300 import inputs as fin  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = 10.0 + 5.0 * rank
+        out[rank] = bench.max_over_ranks(ms, world, torch.device("cpu"))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_slowest_rank_time_over_gloo():
+    world = 2
+    ctx = torch.multiprocessing.get_context("spawn")
+    out = ctx.Manager().dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert dict(out) == {0: 15.0, 1: 15.0}
+
+
+def test_ranks_get_independent_batches_of_one_shape():
+    w = fin.custom(1, 2, 64, 64, False, seed=9)
+    w0, w1 = bench.rank_workload(w, 0, 2), bench.rank_workload(w, 1, 2)
+    assert (w0.B, w0.H, w0.N, w0.d) == (w1.B, w1.H, w1.N, w1.d)
+    assert w0.seed != w1.seed
+    assert bench.rank_workload(w, 0, 1) is w
+    x0, x1 = fin.make_inputs(w0), fin.make_inputs(w1)
+    assert not (x0.q == x1.q).all()
+
+
+def test_throughput_counts_every_rank():
+    assert bench.job_throughput(1, 10, 1e12, 1000.0) == pytest.approx(10.0)
+    assert bench.job_throughput(4, 10, 1e12, 1000.0) == pytest.approx(40.0)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+
+    class Args:
+        steps, warmup = 1, 0
+    assert bench.run_reference(Args(), fin.WORKLOADS["tiny"]) == 0
+    assert capsys.readouterr().out == ""
