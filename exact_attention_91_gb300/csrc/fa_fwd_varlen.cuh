@@ -351,7 +351,7 @@ __device__ __forceinline__ void softmax_role(const VlParams& p, int warp, int la
     const uint32_t tP = tmem + (t == 0 ? Cfg::kTmemP0 : Cfg::kTmemP1) + lane_base;
     const float c_log2 = p.scale_log2;
     uint32_t s_cnt = 0;
-    uint32_t p_made = 0, pv_seen = 0;  // P tiles written / P·V completions observed (early-S mode)
+    uint32_t p_made = 0, pv_seen = 0;  // P tiles written / P·V completions observed
     bool failed = false;
     for (int it = 0;; ++it) {
         const int u = next_unit(sm, it, lane, p);

@@ -455,7 +455,7 @@ __device__ __forceinline__ void ws_softmax_role(const CUtensorMap& tm_o, const F
     const uint32_t stage_s = sm.sbase + Cfg::kOffStage + t * kBoxBytes;
     const float c_log2 = p.scale_log2;
     uint32_t s_cnt = 0;
-    uint32_t p_made = 0, pv_seen = 0;  // P tiles written / P·V completions observed (early-S mode)
+    uint32_t p_made = 0, pv_seen = 0;  // P tiles written / P·V completions observed
     bool failed = false;
     for (int it = 0;; ++it) {
         const int u = next_unit(sm, it, lane, 0xffffffffu, p);
