@@ -185,6 +185,15 @@ def job_throughput(world: int, steps: int, flops_step: float, ms_total: float) -
     return world * steps * flops_step / (ms_total * 1e-3) / 1e12
 
 
+def exp_roofline(w: fin.Workload, launch_s: float, clocks: dict, sm_count: int) -> dict:
+    pairs = w.B * w.H * (w.N * (w.N + 1) // 2 if w.causal else w.N * w.N)
+    mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    peak = 32.0 * sm_count * mhz * 1e6
+    achieved = pairs / launch_s
+    return {"achieved_per_s": achieved, "peak_per_s": peak, "frac": achieved / peak,
+            "exps_per_launch": pairs, "peak_basis": f"32 ex2/clk/SM x {sm_count} SMs x {mhz:.0f} MHz"}
+
+
 def cpu_model() -> str:
     try:
         with open("/proc/cpuinfo", encoding="utf-8") as f:
@@ -306,6 +315,7 @@ def run_ours(args, w: fin.Workload):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     fa.load_library()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
 
     x = fin.make_inputs(rank_workload(w, rank, world))
 
@@ -458,6 +468,10 @@ def run_ours(args, w: fin.Workload):
                 "bytes_per_launch": w.hbm_bytes,
                 "note": "compulsory bytes (Q, K, V read, O and LSE written) over the kernel time"},
         "warm_l2_ms_per_step": warm_ms,
+        # the second ceiling: one ex2 per (query, visible key); MUFU issues 32
+        # ex2 per clock per SM on GB300 (a probe of back-to-back ex2 measured
+        # ~29 per clock per SM), at the median SM clock of the timed region
+        "exp_roofline": exp_roofline(w, avg_launch_s, clocks, sm_count),
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
