@@ -67,8 +67,12 @@ typedef enum fa_status {
  * allocated and zeroed by the first fa_fwd call on that device (that first
  * call synchronises the device) and kept until the process exits. Each
  * launch uses one of its 64 counter slots in turn and leaves it zeroed, so up
- * to 64 launches may be in flight at once on different streams. The call is
- * asynchronous: argument errors
+ * to 64 launches may be in flight at once on different streams. A non-causal
+ * problem with few work units per SM splits each unit's key range in 2-4
+ * parts; such a call also takes a scratch buffer for the partial results
+ * (about nsplit * B*H*N*(d+1)*4 bytes) from a stream-ordered memory pool that
+ * the library creates per device, and frees it on `stream` after its kernel
+ * (fa_fwd_noalloc never splits). The call is asynchronous: argument errors
  * are returned before anything is queued; faults inside the kernel appear at
  * the caller's next synchronisation, and a kernel that gave up on a wait
  * leaves its O/LSE rows unwritten and reports through fa_device_status().
