@@ -69,14 +69,15 @@ __device__ __forceinline__ int kv_tiles(int q_tile, int nq, int nk, int off) {
     return kmax < 0 ? 0 : min(kmax / kBlockN + 1, n_k);
 }
 
-// Unit u: the heaviest 256-query blocks first, every sequence and head at one
-// block index together.
+// Unit u: the order of the equal-length kernel (unit_coords): (sequence,
+// head) pairs in groups of 16 so that the K/V tiles in flight stay in L2,
+// and inside a group the latest query blocks first. Blocks past the end of a
+// shorter sequence are skipped when claimed.
 template <bool CAUSAL>
 __device__ __forceinline__ Item item_coords(int u, const Geometry& g, const VlParams& p) {
     Item w;
     w.unit = u;
-    w.qb = g.nqb - 1 - u / g.BH;
-    w.bh = u - (u / g.BH) * g.BH;
+    unit_coords(u, g.nqb, g.BH, w.bh, w.qb);
     const int b = w.bh / p.heads;
     w.head = w.bh - b * p.heads;
     w.q0 = p.cu_q[b];
