@@ -50,13 +50,17 @@ METRIC = "attention fwd TFLOP/s and % of GB300 dense-bf16 peak at 1 GPU"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
+# the sources that build the equal-length kernel (fa_fwd) and its launch; the
+# variable-length kernel (fa_fwd_varlen.cuh) is a separate kernel
+KERNEL_FILES = ("fa_api.cu", "fa_common.cuh", "fa_fwd_ws.cuh", "ptx.cuh")
+
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_91_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_FILES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
