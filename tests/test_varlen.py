@@ -17,6 +17,7 @@ CASES = [
     ([1000, 5, 256, 257], [1000, 900, 128, 300], 2, 128),
     ([1, 1, 1, 1], [4096, 100, 1, 2049], 4, 128),        # decode: one query per sequence
     ([200, 333], [50, 90], 2, 64),                        # more queries than keys
+    ([5, 130, 3], [0, 260, 0], 2, 128),                   # sequences without keys
 ]
 
 
