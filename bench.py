@@ -402,33 +402,61 @@ def run_ours(args, w: fin.Workload):
         stream.synchronize()
         warm_ms = w0.elapsed_time(w1) / args.steps
 
-    # ---- end to end: pinned host buffers, copies inside the timed region
+    # ---- end to end: pinned host buffers, copies inside the timed region.
+    # Every step copies its inputs host->device and reads its result back.
+    # Two device buffer sets let the host->device copy of step i+1 (one
+    # stream) and the device->host read of step i (another) overlap the
+    # kernel of step i (a third), as a serving loop over this API would.
     hq = torch.from_numpy(x.q.view(np.int16)).view(torch.bfloat16).pin_memory()
     hk = torch.from_numpy(x.k.view(np.int16)).view(torch.bfloat16).pin_memory()
     hv = torch.from_numpy(x.v.view(np.int16)).view(torch.bfloat16).pin_memory()
     ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
     hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     e2e_steps = max(1, min(args.steps, 20))
+    sets = [(q, k, v, o, lse),
+            tuple(torch.empty_like(t) for t in (q, k, v, o, lse))]
+    s_h2d = torch.cuda.Stream(device=dev)
+    s_d2h = torch.cuda.Stream(device=dev)
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        launch()
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-    with torch.cuda.stream(stream):
-        e2e_step()
-    stream.synchronize()
+    def e2e_run(n):
+        k_done = [torch.cuda.Event() for _ in range(n)]
+        d_done = [torch.cuda.Event() for _ in range(n)]
+        for i in range(n):
+            bq, bk, bv, bo, bl = sets[i % 2]
+            h_done = torch.cuda.Event()
+            if i >= 2:
+                s_h2d.wait_event(k_done[i - 2])  # kernel i-2 has read this set's inputs
+            with torch.cuda.stream(s_h2d):
+                bq.copy_(hq, non_blocking=True)
+                bk.copy_(hk, non_blocking=True)
+                bv.copy_(hv, non_blocking=True)
+                h_done.record(s_h2d)
+            stream.wait_event(h_done)
+            if i >= 2:
+                stream.wait_event(d_done[i - 2])  # this set's outputs have been read back
+            rc = fa.fa_fwd(bq.data_ptr(), bk.data_ptr(), bv.data_ptr(), bo.data_ptr(), bl.data_ptr(),
+                           B, H, N, d, w.scale, w.causal, sp)
+            if rc != 0:
+                raise fa.FaError(rc)
+            k_done[i].record(stream)
+            s_d2h.wait_event(k_done[i])
+            with torch.cuda.stream(s_d2h):
+                ho.copy_(bo, non_blocking=True)
+                hl.copy_(bl, non_blocking=True)
+                d_done[i].record(s_d2h)
+        return d_done[-1]
+
+    e2e_run(2)
+    torch.cuda.synchronize()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-    stream.synchronize()
+    e0.record(stream)
+    s_h2d.wait_event(e0)
+    last = e2e_run(e2e_steps)
+    stream.wait_event(last)
+    e1.record(stream)
+    torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     sampler.stop()
 
@@ -464,7 +492,10 @@ def run_ours(args, w: fin.Workload):
                      "avg_launch_ms": avg_launch_s * 1e3},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 3 * B * H * N * d * 2,
-                "d2h_bytes_per_step": B * H * N * d * 2 + B * H * N * 4, "steps": e2e_steps},
+                "d2h_bytes_per_step": B * H * N * d * 2 + B * H * N * 4, "steps": e2e_steps,
+                "overlap": "two buffer sets: the H2D copy of step i+1 and the D2H read of step i "
+                           "overlap the kernel of step i (three streams); host->device runs at "
+                           "~190 GB/s, which bounds this number"},
         "gpu_launches": args.steps,
         "hbm": {"achieved_gbs": w.hbm_bytes / avg_launch_s / 1e9,
                 "peak_gbs": float((peaks or {}).get("hbm_gbs", 6800.0)),
