@@ -524,7 +524,10 @@ def run_ours(args, w: fin.Workload):
 #   decode       64 sequences of one query against 8192 keys, H = 32,
 #                d = 128, causal (the last query sees every key): bound by
 #                reading K and V, reported as GB/s of compulsory bytes
-VARLEN_MIXES = ("prefill_mix", "decode")
+#   decode_long  2 sequences of one query against 65536 keys, H = 32,
+#                d = 128, causal: 64 (sequence, head) pairs for 152 SMs, so
+#                each pair's key range is split and merged; GB/s as decode
+VARLEN_MIXES = ("prefill_mix", "decode", "decode_long")
 
 
 def varlen_batch(name: str):
@@ -532,6 +535,8 @@ def varlen_batch(name: str):
     if name == "prefill_mix":
         n = [int(x) for x in g.integers(256, 8193, size=16)]
         return n, n, 32, 128, True
+    if name == "decode_long":
+        return [1] * 2, [65536] * 2, 32, 128, True
     return [1] * 64, [8192] * 64, 32, 128, True
 
 
@@ -590,7 +595,9 @@ def run_varlen(args) -> int:
     sampler.stop()
     ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / args.steps
     peaks = load_peaks() or {}
-    if args.varlen == "decode":
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nsplit = fa.fa_varlen_num_splits(len(sq), H, total_k, max(sq), sms)
+    if args.varlen.startswith("decode"):
         value, unit = bytes_step / (ms * 1e-3) / 1e9, "GB/s"
         peak = float(peaks.get("hbm_gbs", 6800.0))
         roof = {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
@@ -609,7 +616,8 @@ def run_varlen(args) -> int:
         "config": {"workload": f"varlen_{args.varlen}", "B": len(sq), "H": H, "d": d, "causal": causal,
                    "seqlens_q": sq if len(set(sq)) > 1 else f"{len(sq)} x {sq[0]}",
                    "seqlens_k": sk if len(set(sk)) > 1 else f"{len(sk)} x {sk[0]}",
-                   "l2": "inputs larger than L2" if flush is None else "L2 flushed between timed launches"},
+                   "l2": "inputs larger than L2" if flush is None else "L2 flushed between timed launches",
+                   "key_range_splits": nsplit},
         "roofline": roof, "gpu_launches": args.steps, "clocks": sampler.summary(wall0, wall1),
     }
     print(json.dumps(line), flush=True)

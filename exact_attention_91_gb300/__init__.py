@@ -17,10 +17,10 @@ from .build import LIB_PATH
 
 __all__ = ["FaError", "load_library", "fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
            "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_fwd_varlen",
-           "attention_forward", "attention_forward_varlen", "EXPORTED_SYMBOLS"]
+           "fa_varlen_num_splits", "attention_forward", "attention_forward_varlen", "EXPORTED_SYMBOLS"]
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_noalloc", "fa_fwd_varlen", "fa_strerror", "fa_device_status",
-                    "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout")
+                    "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_varlen_num_splits")
 
 FA_OK = 0
 FA_ERR_DEVICE_TIMEOUT = -8
@@ -61,6 +61,8 @@ def load_library(path: str | None = None):
     lib.fa_abi_version.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [vp, ctypes.c_ulonglong]
     lib.fa_selftest_wait_timeout.restype = i
+    lib.fa_varlen_num_splits.argtypes = [i, i, i, i, i]
+    lib.fa_varlen_num_splits.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -89,6 +91,12 @@ def fa_fwd_varlen(q: int, k: int, v: int, o: int, lse: int | None, cu_q: int, cu
     """The C ``fa_fwd_varlen``: device pointers as ints, returns the status code."""
     return load_library().fa_fwd_varlen(q, k, v, o, lse or None, cu_q, cu_k, B, H, total_q, total_k,
                                         max_seqlen_q, d, scale, int(bool(causal)), stream or None)
+
+
+def fa_varlen_num_splits(B: int, H: int, total_k: int, max_seqlen_q: int, sm_count: int) -> int:
+    """The C ``fa_varlen_num_splits`` (host only): work items per unit's key
+    range that ``fa_fwd_varlen`` uses for these sizes, or a negative status."""
+    return load_library().fa_varlen_num_splits(B, H, total_k, max_seqlen_q, sm_count)
 
 
 def fa_strerror(status: int) -> str:

@@ -1,5 +1,6 @@
 // C ABI of libfa.so: argument checks, TMA tensor maps, kernel selection and
 // launch. Declarations and the contract of every entry point are in fa.h.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -148,6 +149,31 @@ int choose_nsplit(long long units, int n_k_tiles, int sms, bool causal) {
     return best;
 }
 
+// Number of splits of each unit's key range in a variable-length batch.
+// Units are (sequence, head, 256-query block); with few of them (decode: one
+// query per sequence) most SMs would sit idle. One CTA streams K/V at about
+// 60 GB/s (measured on GB300, decode at d = 128), so about 0.6 x the SM count
+// of work items in flight reach the HBM limit, and every split beyond that
+// only adds its fixed cost (Q load, pipeline fill, partial write, merge).
+// The count is the fewest splits that give that many items, with at least 4
+// key tiles (by the mean key count per sequence) per split, 64 at most.
+int choose_nsplit_varlen(long long units, long long B, long long total_k, int sms) {
+    const long long kt = (total_k / B + fa::kBlockN - 1) / fa::kBlockN;  // mean key tiles per sequence
+    if (sms <= 0 || units <= 0 || kt < 8) return 1;
+    const long long target = (6LL * sms + 9) / 10;
+    if (units >= target) return 1;
+    const long long want = (target + units - 1) / units;
+    return static_cast<int>(std::max<long long>(1, std::min<long long>({want, kt / 4, 64})));
+}
+
+// choose_nsplit_varlen, lowered until the unit counter holds every item plus
+// one over-claim per CTA.
+int varlen_splits(long long units, long long B, long long total_k, int sms) {
+    int sp = choose_nsplit_varlen(units, B, total_k, sms);
+    while (sp > 1 && units * sp > 0x7fffffffLL - 65536) --sp;
+    return sp;
+}
+
 // 3-D view [B*H][N][d] of a contiguous bf16 [B,H,N,d] tensor, boxes of
 // 128 rows x 64 columns (128 bytes, 128-byte swizzle). Rows past N inside a
 // head read as zero and are not written by stores.
@@ -251,7 +277,7 @@ int launch_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
         }
     }
     const long long nqb = (static_cast<long long>(prm.max_nq) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-    const long long items = nqb * prm.num_heads_total;
+    const long long items = nqb * prm.num_heads_total * prm.nsplit;
     const unsigned grid = static_cast<unsigned>(items < sm_count ? items : sm_count);
     kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, prm);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
@@ -393,6 +419,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return rc;
 }
 
+int fa_varlen_num_splits(int B, int H, int total_k, int max_seqlen_q, int sm_count) {
+    if (B < 1 || H < 1 || total_k < 0 || max_seqlen_q < 0 || sm_count < 1) return FA_ERR_BAD_SHAPE;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long nqb = (static_cast<long long>(max_seqlen_q) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+    if (BH > 0x7fffffffLL || BH * nqb > 0x7fffffffLL - 65536) return FA_ERR_BAD_SHAPE;
+    return varlen_splits(BH * nqb, B, total_k, sm_count);
+}
+
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
                   const int* cu_seqlens_k, int B, int H, int total_q, int total_k, int max_seqlen_q, int d,
                   float scale, int causal, void* stream) {
@@ -405,8 +439,9 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
     const long long BH = static_cast<long long>(B) * H;
     const long long nqb = (static_cast<long long>(max_seqlen_q) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-    // (element offsets are 64-bit; token indices and the unit count must fit in int)
-    if (BH > 0x7fffffffLL || BH * nqb > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
+    // (element offsets are 64-bit; token indices and the unit count, plus one
+    // over-claim per CTA, must fit in int)
+    if (BH > 0x7fffffffLL || BH * nqb > 0x7fffffffLL - 65536) return FA_ERR_BAD_SHAPE;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
     if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||
@@ -451,11 +486,45 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
     prm.sched = st->sched + (st->sched_next.fetch_add(1) % kSchedSlots) * kSchedSlotWords;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int sms = st->sm_count;
+    const long long units = BH * nqb;
+    prm.nsplit = varlen_splits(units, B, total_k, sms);
+    void* scratch = nullptr;
+    if (prm.nsplit > 1) {
+        // per call, stream-ordered: [partial O | partial LSE | tickets], only
+        // for the query rows that can exist (max_seqlen_q of them per unit at most)
+        prm.part_tiles = max_seqlen_q > fa::kBlockM ? 2 : 1;
+        prm.part_rows = max_seqlen_q < fa::kBlockM ? max_seqlen_q : fa::kBlockM;
+        const size_t rows = static_cast<size_t>(units) * prm.nsplit * prm.part_tiles * prm.part_rows;
+        const size_t o_bytes = rows * d * sizeof(float);
+        const size_t l_bytes = rows * sizeof(float);
+        const size_t t_bytes = static_cast<size_t>(units) * 2 * sizeof(unsigned);
+        if (ensure_pool(dev, *st) != FA_OK ||
+            cudaMallocFromPoolAsync(&scratch, o_bytes + l_bytes + t_bytes, st->pool, s) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_LAUNCH;
+        }
+        prm.part_o = static_cast<float*>(scratch);
+        prm.part_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
+        prm.tickets = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + o_bytes + l_bytes);
+        if (cudaMemsetAsync(prm.tickets, 0, t_bytes, s) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFreeAsync(scratch, s);
+            return FA_ERR_LAUNCH;
+        }
+    } else {
+        prm.nsplit = 1;
+    }
     if (d == 64)
-        return causal ? launch_varlen<64, true>(tq, tk, tv, prm, dev, sms, s)
-                      : launch_varlen<64, false>(tq, tk, tv, prm, dev, sms, s);
-    return causal ? launch_varlen<128, true>(tq, tk, tv, prm, dev, sms, s)
-                  : launch_varlen<128, false>(tq, tk, tv, prm, dev, sms, s);
+        rc = causal ? launch_varlen<64, true>(tq, tk, tv, prm, dev, sms, s)
+                    : launch_varlen<64, false>(tq, tk, tv, prm, dev, sms, s);
+    else
+        rc = causal ? launch_varlen<128, true>(tq, tk, tv, prm, dev, sms, s)
+                    : launch_varlen<128, false>(tq, tk, tv, prm, dev, sms, s);
+    if (scratch && cudaFreeAsync(scratch, s) != cudaSuccess) {
+        cudaGetLastError();
+        if (rc == FA_OK) rc = FA_ERR_LAUNCH;
+    }
+    return rc;
 }
 
 }  // extern "C"

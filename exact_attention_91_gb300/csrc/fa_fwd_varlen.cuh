@@ -14,7 +14,12 @@
 //     with Nq = Nk it is the usual one); a query tile whose queries see no key
 //     issues no MMA, and such queries get O = 0, LSE = -inf;
 //   * O rows are written with 16-byte stores (a TMA box would run into the next
-//     sequence), only inside [0, total_q).
+//     sequence), only inside [0, total_q);
+//   * when there are few units (decode: a handful of sequences with one query
+//     each and long key sets), each unit's key tiles are split among `nsplit`
+//     work items; every item writes its normalised partial O and base-2 LSE
+//     for the rows that exist, and the last item of a tile to finish merges
+//     them (O = sum_s w_s O_s, w_s = 2^(L_s - L) with L the merged LSE).
 // ("Mini FlashAttention", §4 "The flash trick: online softmax", checks its
 // loop on ragged sequences.)
 #pragma once
@@ -36,22 +41,30 @@ struct VlParams {
     float scale_log2;     // scale * log2(e)
     unsigned long long wait_limit_ns;
     unsigned* sched;      // work-queue slot {next unit, CTAs finished}
+    // Key-range split; nsplit = 1: none, and the four fields below are unused.
+    int nsplit;
+    int part_tiles;       // query tiles per item that can hold a query: min(2, ceil(max_nq / 128))
+    int part_rows;        // rows kept per tile: min(128, max_nq)
+    float* part_o;        // [items][part_tiles][d/4][part_rows][4] fp32: normalised partial O
+    float* part_lse;      // [items][part_tiles][part_rows] fp32: base-2 LSE of each partial
+    unsigned* tickets;    // [units][2], zero at launch: items of a tile finished so far
 };
 
 struct Geometry {
-    int BH, nqb, n_items;
+    int BH, nqb, nsplit, n_items;
     __device__ __forceinline__ explicit Geometry(const VlParams& p) {
         BH = p.num_heads_total;
         nqb = (p.max_nq + 2 * kBlockM - 1) / (2 * kBlockM);
-        n_items = nqb * BH;
+        nsplit = p.nsplit;
+        n_items = nqb * BH * nsplit;
     }
 };
 
-// One unit: sequence b, head h (bh = b*H + h), query block qb; its queries are
-// tokens q0 .. q0+nq-1 and its keys k0 .. k0+nk-1; query tile t visits key
-// tiles 0 .. n_t-1 (jb = 0: the key range is never split).
+// One work item: split `split` of unit `unit` = (sequence b, head h, bh =
+// b*H + h, query block qb); its queries are tokens q0 .. q0+nq-1 and its keys
+// k0 .. k0+nk-1; query tile t visits key tiles jb .. jb+n_t-1.
 struct Item {
-    int unit, bh, qb, jb, n0, n1;
+    int unit, split, bh, qb, jb, n0, n1;
     int head, q0, nq, k0, nk, off;  // off = nk - nq
     __device__ __forceinline__ int n_load() const { return n0 > n1 ? n0 : n1; }
 };
@@ -69,15 +82,23 @@ __device__ __forceinline__ int kv_tiles(int q_tile, int nq, int nk, int off) {
     return kmax < 0 ? 0 : min(kmax / kBlockN + 1, n_k);
 }
 
-// Unit u: the order of the equal-length kernel (unit_coords): (sequence,
-// head) pairs in groups of 16 so that the K/V tiles in flight stay in L2,
-// and inside a group the latest query blocks first. Blocks past the end of a
-// shorter sequence are skipped when claimed.
+// Item u: unit u / nsplit in the order of the equal-length kernel
+// (unit_coords): (sequence, head) pairs in groups of 16 so that the K/V tiles
+// in flight stay in L2, and inside a group the latest query blocks first.
+// Blocks past the end of a shorter sequence are skipped when claimed. Split s
+// takes the s-th of nsplit contiguous shares of the key tiles that the unit
+// loads; a tile that sees fewer keys takes what of its own range falls there.
 template <bool CAUSAL>
 __device__ __forceinline__ Item item_coords(int u, const Geometry& g, const VlParams& p) {
     Item w;
-    w.unit = u;
-    unit_coords(u, g.nqb, g.BH, w.bh, w.qb);
+    if (g.nsplit == 1) {
+        w.unit = u;
+        w.split = 0;
+    } else {
+        w.unit = u / g.nsplit;
+        w.split = u - w.unit * g.nsplit;
+    }
+    unit_coords(w.unit, g.nqb, g.BH, w.bh, w.qb);
     const int b = w.bh / p.heads;
     w.head = w.bh - b * p.heads;
     w.q0 = p.cu_q[b];
@@ -88,6 +109,13 @@ __device__ __forceinline__ Item item_coords(int u, const Geometry& g, const VlPa
     w.jb = 0;
     w.n0 = kv_tiles<CAUSAL>(2 * w.qb, w.nq, w.nk, w.off);
     w.n1 = kv_tiles<CAUSAL>(2 * w.qb + 1, w.nq, w.nk, w.off);
+    if (g.nsplit > 1) {
+        const int n = w.n_load();
+        const int je = (w.split + 1) * n / g.nsplit;
+        w.jb = w.split * n / g.nsplit;
+        w.n0 = max(0, min(je, w.n0) - w.jb);
+        w.n1 = max(0, min(je, w.n1) - w.jb);
+    }
     return w;
 }
 
@@ -512,20 +540,93 @@ __device__ __forceinline__ void softmax_role(const VlParams& p, int warp, int la
                 dst[q8] = v;
             }
         };
-#pragma unroll
-        for (int b = 0; b < D / kBoxCols; ++b) {
-            float o[64];
+        // this row's final (or, with a split key range, partial) O: fp32 f[0..63] of box b
+        auto row_box = [&](int b, float (&f)[64]) {
             if (n_t > 0) {
-                load_row64(tO + b * 64, o);
+                load_row64(tO + b * 64, f);
             } else {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) o[i] = 0.f;  // O holds nothing of this unit
+                for (int i = 0; i < 64; ++i) f[i] = 0.f;  // O holds nothing of this item
             }
 #pragma unroll
-            for (int i = 0; i < 64; ++i) o[i] *= inv_l;
-            store_cols(b, o);
+            for (int i = 0; i < 64; ++i) f[i] *= inv_l;
+        };
+        bool write_out = true;
+        if (g.nsplit == 1) {
+#pragma unroll
+            for (int b = 0; b < D / kBoxCols; ++b) {
+                float o[64];
+                row_box(b, o);
+                store_cols(b, o);
+            }
+        } else if (i0 < seq_nq) {  // (the same for every split of the unit and every thread of the tile)
+            // Publish this split's O and LSE for the rows that exist, take a
+            // ticket, and let the last split of the tile merge all of them.
+            const int R = p.part_rows;
+            const size_t tile_slot = static_cast<size_t>(u) * p.part_tiles + t;  // (item, tile)
+            float* po = p.part_o + tile_slot * R * D;
+#pragma unroll
+            for (int b = 0; b < D / kBoxCols; ++b) {
+                float o[64];
+                row_box(b, o);
+                if (row_in) {
+#pragma unroll
+                    for (int cg = 0; cg < 16; ++cg)
+                        __stcg(reinterpret_cast<float4*>(po + (static_cast<size_t>(b * 16 + cg) * R + row) * 4),
+                               make_float4(o[cg * 4], o[cg * 4 + 1], o[cg * 4 + 2], o[cg * 4 + 3]));
+                }
+            }
+            if (row_in) __stcg(p.part_lse + tile_slot * R + row, lse2);
+            __threadfence();
+            ptx::named_bar_sync(1 + t, 128);
+            if (row == 0) {
+                const unsigned done = atomicAdd(p.tickets + static_cast<size_t>(w.unit) * 2 + t, 1u);
+                *sm.last_flag(t) = (done == static_cast<unsigned>(g.nsplit - 1)) ? 1 : 0;
+            }
+            ptx::named_bar_sync(1 + t, 128);
+            write_out = *sm.last_flag(t) != 0;
+            if (write_out && row_in) {
+                __threadfence();
+                // O = sum_s 2^(L_s - M) O_s / sum_s 2^(L_s - M), LSE = M + log2(sum);
+                // a split where the row sees no key has L_s = -inf and weight 0
+                const size_t first = static_cast<size_t>(w.unit) * g.nsplit * p.part_tiles + t;  // split 0
+                const size_t step = static_cast<size_t>(p.part_tiles);
+                float mmax = -INFINITY;
+                for (int sp = 0; sp < g.nsplit; ++sp)
+                    mmax = fmaxf(mmax, __ldcg(p.part_lse + (first + sp * step) * R + row));
+                const bool seen = mmax != -INFINITY;  // the row sees some key in some split
+                const float m_w = seen ? mmax : 0.f;
+                float wsum = 0.f;
+                for (int sp = 0; sp < g.nsplit; ++sp)
+                    wsum += ptx::ex2_approx(__ldcg(p.part_lse + (first + sp * step) * R + row) - m_w);
+                const float inv_w = seen ? 1.0f / wsum : 0.f;
+#pragma unroll 1
+                for (int b = 0; b < D / kBoxCols; ++b) {
+                    float acc[64];
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+                    for (int sp = 0; sp < g.nsplit; ++sp) {
+                        const size_t slot = first + sp * step;
+                        const float wgt = ptx::ex2_approx(__ldcg(p.part_lse + slot * R + row) - m_w) * inv_w;
+                        const float* ps = p.part_o + slot * R * D;
+#pragma unroll
+                        for (int cg = 0; cg < 16; ++cg) {
+                            const float4 v =
+                                __ldcg(reinterpret_cast<const float4*>(ps + (static_cast<size_t>(b * 16 + cg) * R + row) * 4));
+                            acc[cg * 4] = fmaf(wgt, v.x, acc[cg * 4]);
+                            acc[cg * 4 + 1] = fmaf(wgt, v.y, acc[cg * 4 + 1]);
+                            acc[cg * 4 + 2] = fmaf(wgt, v.z, acc[cg * 4 + 2]);
+                            acc[cg * 4 + 3] = fmaf(wgt, v.w, acc[cg * 4 + 3]);
+                        }
+                    }
+                    store_cols(b, acc);
+                }
+                lse2 = seen ? mmax + log2f(wsum) : -INFINITY;
+            }
+        } else {
+            write_out = false;  // no query of the sequence in this tile
         }
-        if (p.lse != nullptr && row_in) p.lse[lse_idx] = lse2 * 0.69314718055994531f;
+        if (write_out && p.lse != nullptr && row_in) p.lse[lse_idx] = lse2 * 0.69314718055994531f;
         ptx::tc_fence_before_sync();
     }
 }

@@ -132,14 +132,31 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
  *          sees every key. A query that sees no key gets O = 0, LSE = -inf.
  *
  * Same return codes as fa_fwd (FA_ERR_BAD_SHAPE for negative totals,
- * max_seqlen_q > total_q, or B*H*ceil(max_seqlen_q/256) >= 2^31; q/o and k/v
- * may be NULL when total_q, resp. total_k, is 0); a batch with no query
- * returns FA_OK at once. The
- * key range of a unit is never split (no scratch memory is used).
+ * max_seqlen_q > total_q, or B*H*ceil(max_seqlen_q/256) >= 2^31 - 65536; q/o
+ * and k/v may be NULL when total_q, resp. total_k, is 0); a batch with no
+ * query returns FA_OK at once.
+ *
+ * Work is split into units of (sequence, head, 256 queries). When there are
+ * few units for the GPU's SMs (decode: a few sequences of one query against
+ * long key sets), each unit's key tiles are divided among several work items
+ * (fa_varlen_num_splits gives how many). Each item writes its partial O,
+ * normalised, and its LSE to scratch memory, and the last item of a unit to
+ * finish merges them: O = sum_s 2^(L_s - L) O_s with L = log2 sum_s 2^L_s
+ * (base-2 LSEs), the online-softmax rescaling applied across items. The
+ * scratch memory comes, stream-ordered, from the same device memory pool as
+ * fa_fwd's.
  */
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                   const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H, int total_q,
                   int total_k, int max_seqlen_q, int d, float scale, int causal, void* stream);
+
+/*
+ * fa_varlen_num_splits — host-only, no device call: how many work items
+ * fa_fwd_varlen gives each unit's key range for these sizes on a GPU with
+ * `sm_count` SMs (1 = no split). Returns FA_ERR_BAD_SHAPE under the same
+ * shape rules as fa_fwd_varlen, or when sm_count < 1.
+ */
+int fa_varlen_num_splits(int B, int H, int total_k, int max_seqlen_q, int sm_count);
 
 /* Static English text for a return code (never NULL). */
 const char* fa_strerror(int status);

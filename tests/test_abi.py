@@ -95,3 +95,21 @@ def test_varlen_bad_arguments_are_rejected_before_launch(lib):
     assert f(p, p, p, p + 4096, None, p, p, 1, 2, 8, 8, 8, 64, 0.0, 0, None) == -9
     assert f(p + 2, p, p, p + 4096, None, p, p, 1, 2, 8, 8, 8, 64, 0.125, 0, None) == -4
     assert f(p, p, p, p + 64, None, p, p, 1, 2, 8, 8, 8, 64, 0.125, 0, None) == -10  # o overlaps q
+
+
+def test_varlen_split_choice(lib):
+    """fa_varlen_num_splits (host only): the key range of a unit is split only
+    when the units are too few for the SMs and the key sets are long, and
+    every split keeps at least 4 key tiles of 128."""
+    f = lib.fa_varlen_num_splits
+    #        B   H   total_k        max_seqlen_q  SMs
+    assert f(64, 32, 64 * 8192, 1, 152) == 1        # decode, 2048 (sequence, head) pairs: enough units
+    assert f(16, 32, 16 * 4096, 4096, 152) == 1     # prefill-sized units
+    assert f(1, 8, 32768, 1, 152) > 4               # 8 pairs of one query and 32768 keys
+    assert f(2, 4, 2 * 896, 1, 152) == 1            # short key sets: fewer than 8 tiles per sequence
+    for B, H, nk in [(1, 8, 32768), (4, 4, 6000), (1, 2, 3000), (2, 1, 1 << 20)]:
+        sp = f(B, H, B * nk, 1, 152)
+        assert 1 <= sp <= 64 and (sp == 1 or -(-nk // 128) // sp >= 4), (B, H, nk, sp)
+    # splits fill more SMs: 8 units never split into fewer than 152 items' worth of tiles
+    assert f(1, 8, 32768, 1, 152) * 8 <= 2 * 152
+    assert f(0, 8, 100, 1, 152) == -2 and f(1, 8, 100, 1, 0) == -2 and f(1, 8, -1, 1, 152) == -2

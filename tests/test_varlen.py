@@ -18,7 +18,14 @@ CASES = [
     ([1, 1, 1, 1], [4096, 100, 1, 2049], 4, 128),        # decode: one query per sequence
     ([200, 333], [50, 90], 2, 64),                        # more queries than keys
     ([5, 130, 3], [0, 260, 0], 2, 128),                   # sequences without keys
+    # few units for the SMs: each unit's key range is split and merged
+    ([1, 1], [20000, 9000], 4, 128),                      # decode, long key sets
+    ([1, 1, 1], [5000, 16384, 77], 2, 64),                # decode; one key set shorter than a split
+    ([3000], [3000], 2, 128),                             # one long sequence (causal: empty splits)
+    ([4, 200], [12000, 9000], 2, 64),                     # a few queries against long key sets
+    ([1500], [1200], 1, 64),                              # queries that see no key, split
 ]
+SPLIT_CASES = range(5, 10)
 
 
 def _run(x, H, d, causal):
@@ -51,6 +58,19 @@ def test_varlen_matches_oracle(oracle_mod, case, causal):
     assert d_o.max() <= O_MAX_ABS and d_o.mean() <= O_MEAN_ABS
     if (~none).any():
         assert np.abs(lse[~none] - lse_ref[~none]).max() <= LSE_MAX_ABS
+
+
+def test_split_cases_are_split():
+    """The last cases of CASES do run with a split key range on this GPU."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_attention_91_gb300 as fa
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for c in SPLIT_CASES:
+        sq, sk, H, d = CASES[c]
+        assert fa.fa_varlen_num_splits(len(sq), H, sum(sk), max(sq), sms) > 1, c
+    assert fa.fa_varlen_num_splits(len(CASES[2][0]), CASES[2][2], sum(CASES[2][1]), 1, sms) > 1
 
 
 def test_equal_lengths_match_fa_fwd():
