@@ -26,19 +26,26 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
 
 // Work-queue slots of the persistent kernel: {next unit, CTAs finished},
-// one 128-byte line each. A launch takes the next slot of the ring, finds it
-// zero and leaves it zero; 64 slots let that many launches be in flight on
-// different streams without sharing one.
+// one 128-byte line each. A launch finds its slot zero and leaves it zero.
+// Ordinary launches take the next of 64 slots in turn, so that many may be in
+// flight on different streams without sharing one. A launch captured into a
+// CUDA graph keeps the slot it drew at capture for every replay; it draws
+// from 192 further slots that no ordinary launch uses, so a replay never
+// shares one with an ordinary launch, nor with another captured launch until
+// 192 more have been captured.
 constexpr int kSchedSlots = 64;
+constexpr int kGraphSlots = 192;
 constexpr int kSchedSlotWords = 32;
 
 struct DeviceState {
     bool probed = false;
     int status = FA_OK;  // FA_OK, FA_ERR_UNSUPPORTED_ARCH
     int sm_count = 0;
-    unsigned* sched = nullptr;  // kSchedSlots x kSchedSlotWords, allocated on first use
+    unsigned* sched = nullptr;  // (kSchedSlots + kGraphSlots) x kSchedSlotWords, allocated on first use
     std::atomic<unsigned> sched_next{0};
+    std::atomic<unsigned> graph_next{0};
     cudaMemPool_t pool = nullptr;  // stream-ordered scratch for key-range splits
+    std::atomic<bool> kernels_ready{false};  // shared-memory attributes of every kernel set
 };
 DeviceState g_devices[kMaxDevices];
 
@@ -48,7 +55,7 @@ int ensure_sched(DeviceState& st) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (st.sched) return FA_OK;
     void* ptr = nullptr;
-    const size_t bytes = sizeof(unsigned) * kSchedSlots * kSchedSlotWords;
+    const size_t bytes = sizeof(unsigned) * (kSchedSlots + kGraphSlots) * kSchedSlotWords;
     if (cudaMalloc(&ptr, bytes) != cudaSuccess) {
         cudaGetLastError();
         return FA_ERR_LAUNCH;
@@ -217,18 +224,7 @@ int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
               const fa::FwdParams& prm, int dev, int sm_count, cudaStream_t stream) {
     using Cfg = fa::WsCfg<D>;
     auto kernel = fa::fa_fwd_ws_kernel<D, CAUSAL>;
-    static bool attr_set[kMaxDevices] = {};
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
-                cudaSuccess) {
-                cudaGetLastError();
-                return FA_ERR_LAUNCH;
-            }
-            attr_set[dev] = true;
-        }
-    }
+    (void)dev;
     const long long nqb = (static_cast<long long>(prm.N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
     const long long items = nqb * prm.num_heads_total * (prm.nsplit > 1 ? prm.nsplit : 1);
     const unsigned grid = static_cast<unsigned>(items < sm_count ? items : sm_count);
@@ -240,6 +236,67 @@ template <int D, bool CAUSAL>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
            const fa::FwdParams& prm, int dev, int sm_count, cudaStream_t stream) {
     return launch_ws<D, CAUSAL>(tq, tk, tv, to, prm, dev, sm_count, stream);
+}
+
+template <typename Kernel>
+bool set_smem_attr(Kernel kernel, int bytes) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess) return true;
+    cudaGetLastError();
+    return false;
+}
+
+// The dynamic shared memory size of every kernel, set once per device (with
+// that device current) by its first call that is not being captured.
+int prepare_kernels(DeviceState& st) {
+    if (st.kernels_ready.load(std::memory_order_acquire)) return FA_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (st.kernels_ready.load(std::memory_order_relaxed)) return FA_OK;
+    const int b64 = fa::WsCfg<64>::kSmemBytes, b128 = fa::WsCfg<128>::kSmemBytes;
+    const bool ok = set_smem_attr(fa::fa_fwd_ws_kernel<64, false>, b64) &&
+                    set_smem_attr(fa::fa_fwd_ws_kernel<64, true>, b64) &&
+                    set_smem_attr(fa::fa_fwd_ws_kernel<128, false>, b128) &&
+                    set_smem_attr(fa::fa_fwd_ws_kernel<128, true>, b128) &&
+                    set_smem_attr(fa::vl::fa_fwd_varlen_kernel<64, false>, b64) &&
+                    set_smem_attr(fa::vl::fa_fwd_varlen_kernel<64, true>, b64) &&
+                    set_smem_attr(fa::vl::fa_fwd_varlen_kernel<128, false>, b128) &&
+                    set_smem_attr(fa::vl::fa_fwd_varlen_kernel<128, true>, b128);
+    if (!ok) return FA_ERR_LAUNCH;
+    st.kernels_ready.store(true, std::memory_order_release);
+    return FA_OK;
+}
+
+// Whether `stream` is being captured into a CUDA graph (-1: the query failed,
+// or the capture was already invalidated).
+int capturing(cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (cs == cudaStreamCaptureStatusNone) return 0;
+    return cs == cudaStreamCaptureStatusActive ? 1 : -1;
+}
+
+// The work-queue slot (and, on the first ordinary call, the device's launch
+// setup: kernel attributes, the slot ring, the split-scratch pool) of a
+// launch on `stream`. While the stream is captured nothing is allocated or
+// set: the device must have had an ordinary call before.
+int take_sched_slot(int dev, DeviceState& st, cudaStream_t stream, unsigned** slot) {
+    const int cap = capturing(stream);
+    if (cap < 0) return FA_ERR_LAUNCH;
+    if (cap == 0) {
+        if (prepare_kernels(st) != FA_OK || ensure_sched(st) != FA_OK || ensure_pool(dev, st) != FA_OK)
+            return FA_ERR_LAUNCH;
+        *slot = st.sched + (st.sched_next.fetch_add(1) % kSchedSlots) * kSchedSlotWords;
+        return FA_OK;
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!st.kernels_ready.load(std::memory_order_relaxed) || st.sched == nullptr || st.pool == nullptr)
+            return FA_ERR_LAUNCH;
+    }
+    *slot = st.sched + (kSchedSlots + st.graph_next.fetch_add(1) % kGraphSlots) * kSchedSlotWords;
+    return FA_OK;
 }
 
 // One warp waits on an mbarrier phase that nothing completes, through the
@@ -264,18 +321,7 @@ int launch_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
                   const fa::vl::VlParams& prm, int dev, int sm_count, cudaStream_t stream) {
     using Cfg = fa::WsCfg<D>;
     auto kernel = fa::vl::fa_fwd_varlen_kernel<D, CAUSAL>;
-    static bool attr_set[kMaxDevices] = {};
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
-                cudaSuccess) {
-                cudaGetLastError();
-                return FA_ERR_LAUNCH;
-            }
-            attr_set[dev] = true;
-        }
-    }
+    (void)dev;
     const long long nqb = (static_cast<long long>(prm.max_nq) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
     const long long items = nqb * prm.num_heads_total * prm.nsplit;
     const unsigned grid = static_cast<unsigned>(items < sm_count ? items : sm_count);
@@ -379,9 +425,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         std::lock_guard<std::mutex> lock(g_mu);
         prm.wait_limit_ns = g_wait_limit_ns;
     }
-    if (ensure_sched(*st) != FA_OK) return FA_ERR_LAUNCH;
-    prm.sched = st->sched + (st->sched_next.fetch_add(1) % kSchedSlots) * kSchedSlotWords;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (take_sched_slot(dev, *st, s, &prm.sched) != FA_OK) return FA_ERR_LAUNCH;
     const int sms = st->sm_count;
     const long long units = ((static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM)) * BH;
     const int n_k_tiles = static_cast<int>((static_cast<long long>(N) + fa::kBlockN - 1) / fa::kBlockN);
@@ -482,9 +527,8 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
         std::lock_guard<std::mutex> lock(g_mu);
         prm.wait_limit_ns = g_wait_limit_ns;
     }
-    if (ensure_sched(*st) != FA_OK) return FA_ERR_LAUNCH;
-    prm.sched = st->sched + (st->sched_next.fetch_add(1) % kSchedSlots) * kSchedSlotWords;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (take_sched_slot(dev, *st, s, &prm.sched) != FA_OK) return FA_ERR_LAUNCH;
     const int sms = st->sm_count;
     const long long units = BH * nqb;
     prm.nsplit = varlen_splits(units, B, total_k, sms);
@@ -601,6 +645,13 @@ extern "C" int fa_fwd_noalloc(const void* q, const void* k, const void* v, void*
     if (rc != FA_OK) return rc;
     unsigned* scratch = nullptr;
     if (noalloc_scratch(dev, &scratch) != FA_OK) return FA_ERR_LAUNCH;
+    {
+        // kernel attributes are set by an ordinary call, never during a capture
+        const int cap = capturing(static_cast<cudaStream_t>(stream));
+        if (cap < 0) return FA_ERR_LAUNCH;
+        if (cap == 0 ? prepare_kernels(*st) != FA_OK : !st->kernels_ready.load(std::memory_order_acquire))
+            return FA_ERR_LAUNCH;
+    }
 
     CUtensorMap tq, tk, tv, to;
     const int bh = static_cast<int>(BH);

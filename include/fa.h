@@ -62,12 +62,13 @@ typedef enum fa_status {
  * stream   cudaStream_t to run on, as void*; NULL = legacy default stream.
  *
  * Ownership: the caller allocates and owns every buffer; the library keeps
- * no pointer after the call returns. The library's own state is one 8 KB
+ * no pointer after the call returns. The library's own state is one 32 KB
  * device buffer per device (work-queue counters for the persistent kernel),
- * allocated and zeroed by the first fa_fwd call on that device (that first
- * call synchronises the device) and kept until the process exits. Each
- * launch uses one of its 64 counter slots in turn and leaves it zeroed, so up
- * to 64 launches may be in flight at once on different streams. A non-causal
+ * allocated and zeroed by the first fa_fwd or fa_fwd_varlen call on that
+ * device (that first call synchronises the device) and kept until the
+ * process exits. Each launch uses one of its 64 counter slots in turn and
+ * leaves it zeroed, so up to 64 launches may be in flight at once on
+ * different streams. A non-causal
  * problem with few work units per SM splits each unit's key range in 2-4
  * parts; such a call also takes a scratch buffer for the partial results
  * (about nsplit * B*H*N*(d+1)*4 bytes) from a stream-ordered memory pool that
@@ -77,6 +78,23 @@ typedef enum fa_status {
  * the caller's next synchronisation, and a kernel that gave up on a wait
  * leaves its O/LSE rows unwritten and reports through fa_device_status().
  * The current device must be compute capability 10.3 (sm_103a).
+ *
+ * CUDA graphs: fa_fwd, fa_fwd_varlen and fa_fwd_noalloc may be called while
+ * `stream` is being captured (cudaStreamBeginCapture, torch.cuda.graph),
+ * once the device has had one ordinary call of the same entry point: that
+ * call allocates and sets what a capture may not (the counter buffer, the
+ * scratch pool, the kernels' shared-memory sizes). A call captured before
+ * then returns FA_ERR_LAUNCH and enqueues nothing. The tensor maps are
+ * encoded from the pointers given at capture, so a replay reads and writes
+ * those buffers, which must stay allocated while the graph may be replayed
+ * (a replay after one was freed reads or writes unmapped or reused memory;
+ * torch.cuda.graph returns the allocator's free blocks to the driver when a
+ * capture begins). A captured call keeps the counter slot it drew for every
+ * replay, from 192 slots that ordinary calls never use, so replays may
+ * overlap ordinary launches and replays of other graphs on other streams
+ * (until 192 calls have been captured on the device, when the slots wrap);
+ * a key-range split's scratch becomes an allocation node of the graph.
+ * fa_fwd_noalloc's one shared slot stays shared when captured.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, void* stream);
