@@ -495,7 +495,7 @@ def run_ours(args, w: fin.Workload):
                 "d2h_bytes_per_step": B * H * N * d * 2 + B * H * N * 4, "steps": e2e_steps,
                 "overlap": "two buffer sets: the H2D copy of step i+1 and the D2H read of step i "
                            "overlap the kernel of step i (three streams); host->device runs at "
-                           "~190 GB/s, which bounds this number"},
+                           "~211 GB/s (a 1 GB pinned copy on GB300), which bounds this number"},
         "gpu_launches": args.steps,
         "hbm": {"achieved_gbs": w.hbm_bytes / avg_launch_s / 1e9,
                 "peak_gbs": float((peaks or {}).get("hbm_gbs", 6800.0)),
