@@ -18,6 +18,7 @@ CASES = [
     ([1, 1, 1, 1], [4096, 100, 1, 2049], 4, 128),        # decode: one query per sequence
     ([200, 333], [50, 90], 2, 64),                        # more queries than keys
     ([5, 130, 3], [0, 260, 0], 2, 128),                   # sequences without keys
+    ([384, 5], [384, 700], 2, 64),                        # last blocks of <= 128 queries
     # few units for the SMs: each unit's key range is split and merged
     ([1, 1], [20000, 9000], 4, 128),                      # decode, long key sets
     ([1, 1, 1], [5000, 16384, 77], 2, 64),                # decode; one key set shorter than a split
@@ -25,7 +26,7 @@ CASES = [
     ([4, 200], [12000, 9000], 2, 64),                     # a few queries against long key sets
     ([1500], [1200], 1, 64),                              # queries that see no key, split
 ]
-SPLIT_CASES = range(5, 10)
+SPLIT_CASES = range(6, 11)
 
 
 def _run(x, H, d, causal):
