@@ -366,7 +366,7 @@ __device__ __forceinline__ void pv_role(const VlParams& p, int lane, int t) {
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void softmax_role(const VlParams& p, int warp, int lane) {
     using Cfg = WsCfg<D>;
-    constexpr float kTau = 8.0f;
+    constexpr float kTau = 32.0f;  // as in fa_fwd_ws.cuh
     const WsSmem<D> sm;
     const Geometry g(p);
     volatile int* abort_flag = sm.abort_flag();
