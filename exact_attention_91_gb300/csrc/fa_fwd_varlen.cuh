@@ -477,28 +477,34 @@ __device__ __forceinline__ void softmax_role(const VlParams& p, int warp, int la
             }
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;  // fully masked row stays finite
             const float2 cc = make_float2(c_log2, c_log2), mm = make_float2(-m_use, -m_use);
-            float2 sum01 = make_float2(0.f, 0.f), sum23 = make_float2(0.f, 0.f);
-            // p = 2^(S·c - m) and P (bf16 pairs, 64 columns at tP),
-            // one 32-column store per 64 keys as soon as they are done. The
-            // exponent arguments and the running sums use packed fp32 pairs.
+            // p = 2^(S·c - m) and P in three passes over the row, as in fa_fwd_ws.cuh
+#pragma unroll
+            for (int c = 0; c < kBlockN; c += 2) {
+                const float2 x = ptx::ffma2(make_float2(s[c], s[c + 1]), cc, mm);
+                s[c] = x.x;
+                s[c + 1] = x.y;
+            }
+#pragma unroll
+            for (int c = 0; c < kBlockN; ++c) s[c] = ptx::ex2_approx(s[c]);
+            float2 sa = make_float2(0.f, 0.f), sb = sa, sc = sa, sd = sa;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t r[32];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
+                for (int i = 0; i < 32; i += 4) {
                     const int c = h * 64 + 2 * i;
-                    const float2 x01 = ptx::ffma2(make_float2(s[c], s[c + 1]), cc, mm);
-                    const float2 x23 = ptx::ffma2(make_float2(s[c + 2], s[c + 3]), cc, mm);
-                    const float2 p01 = make_float2(ptx::ex2_approx(x01.x), ptx::ex2_approx(x01.y));
-                    const float2 p23 = make_float2(ptx::ex2_approx(x23.x), ptx::ex2_approx(x23.y));
-                    sum01 = ptx::fadd2(sum01, p01);
-                    sum23 = ptx::fadd2(sum23, p23);
-                    r[i] = ptx::pack_bf16x2(p01.x, p01.y);
-                    r[i + 1] = ptx::pack_bf16x2(p23.x, p23.y);
+                    sa = ptx::fadd2(sa, make_float2(s[c], s[c + 1]));
+                    sb = ptx::fadd2(sb, make_float2(s[c + 2], s[c + 3]));
+                    sc = ptx::fadd2(sc, make_float2(s[c + 4], s[c + 5]));
+                    sd = ptx::fadd2(sd, make_float2(s[c + 6], s[c + 7]));
+                    r[i] = ptx::pack_bf16x2(s[c], s[c + 1]);
+                    r[i + 1] = ptx::pack_bf16x2(s[c + 2], s[c + 3]);
+                    r[i + 2] = ptx::pack_bf16x2(s[c + 4], s[c + 5]);
+                    r[i + 3] = ptx::pack_bf16x2(s[c + 6], s[c + 7]);
                 }
                 ptx::tmem_st_32x32b_x32(tP + h * 32, r);
             }
-            const float2 sum = ptx::fadd2(sum01, sum23);
+            const float2 sum = ptx::fadd2(ptx::fadd2(sa, sb), ptx::fadd2(sc, sd));
             l = l * alpha + (sum.x + sum.y);
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
