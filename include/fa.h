@@ -38,7 +38,8 @@ typedef enum fa_status {
     FA_ERR_MISALIGNED = -4,           /* q, k, v, o not 16-byte aligned, or lse not 4-byte aligned */
     FA_ERR_NO_DEVICE = -5,            /* no CUDA device, or the current device cannot be queried */
     FA_ERR_UNSUPPORTED_ARCH = -6,     /* the current device is not compute capability 10.3 */
-    FA_ERR_LAUNCH = -7,               /* tensor-map encoding or the kernel launch failed */
+    FA_ERR_LAUNCH = -7,               /* tensor-map encoding or the kernel launch failed, or a call was
+                                         captured into a CUDA graph before the device's first ordinary call */
     FA_ERR_DEVICE_TIMEOUT = -8,       /* a kernel gave up waiting on an mbarrier (see fa_device_status) */
     FA_ERR_BAD_SCALE = -9,            /* scale is not finite, or not > 0 */
     FA_ERR_ALIAS = -10                /* o or lse overlaps q, k or v, or lse overlaps o */
