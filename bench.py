@@ -262,13 +262,17 @@ class OracleSampler:
 
 # ------------------------------------------------------------------ reference arm
 
+# seconds of oracle work that one `--impl reference` run spends in all
+REFERENCE_BUDGET_S = 120.0
+
+
 def run_reference(args, w: fin.Workload):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     x = fin.make_inputs(w)
     # the whole run (warm-up + timed steps) stays near two minutes of CPU work
-    per_step_s = max(0.005, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    per_step_s = max(0.005, min(20.0, REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)))
     sampler = OracleSampler(w, x, seed=w.seed + 17)
     flops_total = 0.0
     secs_total = 0.0

@@ -67,3 +67,26 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
         steps, warmup = 1, 0
     assert bench.run_reference(Args(), fin.WORKLOADS["tiny"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_rank_zero(monkeypatch, capsys):
+    """Rank 0 of the reference arm prints one JSON line of the bench contract:
+    the oracle's throughput on the same workload, its cores and sample, and an
+    e2e object with no host-device copies."""
+    import json
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", 1.5)
+
+    class Args:
+        steps, warmup = 2, 1
+    assert bench.run_reference(Args(), fin.WORKLOADS["tiny"]) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 2 and d["warmup"] == 1
+    assert d["config"]["workload"] == "tiny" and d["dtype"] == "f64"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
