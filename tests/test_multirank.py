@@ -90,3 +90,23 @@ def test_reference_arm_line_on_rank_zero(monkeypatch, capsys):
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_traffic_is_reported_only_for_the_captured_kernel(monkeypatch, tmp_path):
+    """roofline.traffic comes from the committed ncu capture only while the
+    kernel sources still hash to the captured build; otherwise it is null."""
+    import json
+    t = tmp_path / "traffic.json"
+    t.write_text(json.dumps({"llm_prefill": {"bytes_per_launch": 123, "kernel_sha": bench.kernel_sha()},
+                             "long_sequence": {"bytes_per_launch": 456, "kernel_sha": "0" * 16}}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(t))
+    assert bench.load_traffic("llm_prefill") == 123
+    assert bench.load_traffic("long_sequence") is None      # captured on other kernel sources
+    assert bench.load_traffic("max_shift") is None          # never captured
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "missing.json"))
+    assert bench.load_traffic("llm_prefill") is None
+
+
+def test_committed_traffic_matches_the_current_kernel():
+    """The committed capture belongs to the kernel sources in the tree."""
+    assert bench.load_traffic("llm_prefill") is not None
