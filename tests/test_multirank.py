@@ -105,8 +105,3 @@ def test_traffic_is_reported_only_for_the_captured_kernel(monkeypatch, tmp_path)
     assert bench.load_traffic("max_shift") is None          # never captured
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "missing.json"))
     assert bench.load_traffic("llm_prefill") is None
-
-
-def test_committed_traffic_matches_the_current_kernel():
-    """The committed capture belongs to the kernel sources in the tree."""
-    assert bench.load_traffic("llm_prefill") is not None
