@@ -558,6 +558,7 @@ __device__ __forceinline__ void softmax_role(const VlParams& p, int warp, int la
             for (int i = 0; i < 64; ++i) f[i] *= inv_l;
         };
         bool write_out = true;
+        bool lse_ok = row_in;
         if (g.nsplit == 1) {
 #pragma unroll
             for (int b = 0; b < D / kBoxCols; ++b) {
@@ -565,24 +566,31 @@ __device__ __forceinline__ void softmax_role(const VlParams& p, int warp, int la
                 row_box(b, o);
                 store_cols(b, o);
             }
-        } else if (i0 < seq_nq) {  // (the same for every split of the unit and every thread of the tile)
+        } else if (i0 < seq_nq && t < p.part_tiles) {  // (the same for every split of the unit and every
+                                                       // thread of the tile)
             // Publish this split's O and LSE for the rows that exist, take a
             // ticket, and let the last split of the tile merge all of them.
+            // The scratch holds part_tiles x part_rows rows per item, sized by
+            // max_seqlen_q; a sequence with more queries than that (which the
+            // caller rules out) leaves its extra rows unwritten rather than
+            // writing past its slot.
             const int R = p.part_rows;
+            const bool row_ok = row_in && row < R;
+            lse_ok = row_ok;
             const size_t tile_slot = static_cast<size_t>(u) * p.part_tiles + t;  // (item, tile)
             float* po = p.part_o + tile_slot * R * D;
 #pragma unroll
             for (int b = 0; b < D / kBoxCols; ++b) {
                 float o[64];
                 row_box(b, o);
-                if (row_in) {
+                if (row_ok) {
 #pragma unroll
                     for (int cg = 0; cg < 16; ++cg)
                         __stcg(reinterpret_cast<float4*>(po + (static_cast<size_t>(b * 16 + cg) * R + row) * 4),
                                make_float4(o[cg * 4], o[cg * 4 + 1], o[cg * 4 + 2], o[cg * 4 + 3]));
                 }
             }
-            if (row_in) __stcg(p.part_lse + tile_slot * R + row, lse2);
+            if (row_ok) __stcg(p.part_lse + tile_slot * R + row, lse2);
             __threadfence();
             ptx::named_bar_sync(1 + t, 128);
             if (row == 0) {
@@ -591,7 +599,7 @@ __device__ __forceinline__ void softmax_role(const VlParams& p, int warp, int la
             }
             ptx::named_bar_sync(1 + t, 128);
             write_out = *sm.last_flag(t) != 0;
-            if (write_out && row_in) {
+            if (write_out && row_ok) {
                 __threadfence();
                 // O = sum_s 2^(L_s - M) O_s / sum_s 2^(L_s - M), LSE = M + log2(sum);
                 // a split where the row sees no key has L_s = -inf and weight 0
@@ -632,7 +640,7 @@ __device__ __forceinline__ void softmax_role(const VlParams& p, int warp, int la
         } else {
             write_out = false;  // no query of the sequence in this tile
         }
-        if (write_out && p.lse != nullptr && row_in) p.lse[lse_idx] = lse2 * 0.69314718055994531f;
+        if (write_out && p.lse != nullptr && lse_ok) p.lse[lse_idx] = lse2 * 0.69314718055994531f;
         ptx::tc_fence_before_sync();
     }
 }
