@@ -62,3 +62,25 @@ def test_max_shift_spike():
     s0 = np.einsum("bhic,bhjc->bhij", q0, k) * w.scale
     rise = spike - np.take_along_axis(s0, x.spike_keys[..., None], axis=3)[..., 0]
     assert np.all(np.abs(rise - 20.0) < 0.5)
+
+
+def test_varlen_inputs():
+    """Packed sequences: int32 offsets that start at 0 and add up the counts,
+    token-major [total, H, d] bf16 values, the same bits for the same seed,
+    and empty sequences allowed."""
+    x = fin.make_varlen_inputs([3, 0, 5], [7, 2, 0], 2, 64, seed=9)
+    assert x.cu_q.dtype == np.int32 and x.cu_k.dtype == np.int32
+    assert x.cu_q.tolist() == [0, 3, 3, 8] and x.cu_k.tolist() == [0, 7, 9, 9]
+    assert x.q.shape == (8, 2, 64) and x.k.shape == (9, 2, 64) and x.v.shape == (9, 2, 64)
+    assert x.q.dtype == np.uint16
+    y = fin.make_varlen_inputs([3, 0, 5], [7, 2, 0], 2, 64, seed=9)
+    for a, b in ((x.q, y.q), (x.k, y.k), (x.v, y.v)):
+        np.testing.assert_array_equal(a, b)
+    assert not np.array_equal(x.k, x.v)
+    q, k, v = x.f64()
+    np.testing.assert_array_equal(fin.bf16_from_f64(q), x.q)  # values are exact bf16
+    big = fin.make_varlen_inputs([4000], [4000], 4, 64, seed=10)
+    qb = fin.bf16_to_f64(big.q)
+    assert abs(qb.mean()) < 0.02 and 0.98 < qb.std() < 1.02
+    with pytest.raises(ValueError):
+        fin.make_varlen_inputs([1, 2], [3], 1, 64, seed=1)
