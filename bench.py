@@ -9,7 +9,7 @@ under the causal mask, summed over ranks) with inputs already in HBM, timed
 with CUDA events over exactly K steps between barriers (max over ranks).
 ``e2e`` is the same metric with the inputs copied from pinned host memory
 and O/LSE copied back inside the timed region, through the same C ABI call.
-``roofline`` relates the kernel's average launch time to the measured dense
+``roofline`` relates the kernel's median launch time to the measured dense
 bf16 tensor peak; ``cpu_baseline`` is the fp64 oracle on the host cores over a
 bounded sample of query rows.
 
@@ -50,9 +50,8 @@ METRIC = "attention fwd TFLOP/s and % of GB300 dense-bf16 peak at 1 GPU"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
-# the sources that build the equal-length kernel (fa_fwd) and its launch; the
-# variable-length kernel (fa_fwd_varlen.cuh) is a separate kernel
-KERNEL_FILES = ("fa_api.cu", "fa_common.cuh", "fa_fwd_ws.cuh", "ptx.cuh")
+# the sources that build the forward kernel and its launch
+KERNEL_FILES = ("fa_api.cu", "fa_common.cuh", "fa_fwd_kernel.cuh", "ptx.cuh")
 
 
 def kernel_sha() -> str:
@@ -468,7 +467,10 @@ def run_ours(args, w: fin.Workload):
     value = job_throughput(world, args.steps, flops_step, step_total_ms)
     e2e_value = job_throughput(world, e2e_steps, flops_step, e2e_ms)
     avg_launch_s = kernel_ms / args.steps * 1e-3
-    achieved = flops_step / avg_launch_s / 1e12
+    # the roofline uses the median launch (robust to a launch that met a clock
+    # change or another process's work); the mean is reported beside it
+    median_launch_s = statistics.median(launch_ms) * 1e-3
+    achieved = flops_step / median_launch_s / 1e12
     peaks = load_peaks()
     if peaks and peaks.get("bf16_tflops"):
         peak, peak_src = float(peaks["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
@@ -493,7 +495,8 @@ def run_ours(args, w: fin.Workload):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "kernel": "fa_fwd", "flops_per_launch": flops_step,
-                     "avg_launch_ms": avg_launch_s * 1e3},
+                     "median_launch_ms": median_launch_s * 1e3, "avg_launch_ms": avg_launch_s * 1e3,
+                     "launches_timed": len(launch_ms)},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 3 * B * H * N * d * 2,
                 "d2h_bytes_per_step": B * H * N * d * 2 + B * H * N * 4, "steps": e2e_steps,
@@ -501,16 +504,16 @@ def run_ours(args, w: fin.Workload):
                            "overlap the kernel of step i (three streams); host->device runs at "
                            "~211 GB/s (a 1 GB pinned copy on GB300), which bounds this number"},
         "gpu_launches": args.steps,
-        "hbm": {"achieved_gbs": w.hbm_bytes / avg_launch_s / 1e9,
+        "hbm": {"achieved_gbs": w.hbm_bytes / median_launch_s / 1e9,
                 "peak_gbs": float((peaks or {}).get("hbm_gbs", 6800.0)),
-                "frac": w.hbm_bytes / avg_launch_s / 1e9 / float((peaks or {}).get("hbm_gbs", 6800.0)),
+                "frac": w.hbm_bytes / median_launch_s / 1e9 / float((peaks or {}).get("hbm_gbs", 6800.0)),
                 "bytes_per_launch": w.hbm_bytes,
                 "note": "compulsory bytes (Q, K, V read, O and LSE written) over the kernel time"},
         "warm_l2_ms_per_step": warm_ms,
         # the second ceiling: one ex2 per (query, visible key); MUFU issues 32
         # ex2 per clock per SM on GB300 (a probe of back-to-back ex2 measured
         # ~29 per clock per SM), at the median SM clock of the timed region
-        "exp_roofline": exp_roofline(w, avg_launch_s, clocks, sm_count),
+        "exp_roofline": exp_roofline(w, median_launch_s, clocks, sm_count),
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

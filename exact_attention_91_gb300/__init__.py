@@ -17,10 +17,12 @@ from .build import LIB_PATH
 
 __all__ = ["FaError", "load_library", "fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
            "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_fwd_varlen",
-           "fa_varlen_num_splits", "attention_forward", "attention_forward_varlen", "EXPORTED_SYMBOLS"]
+           "fa_varlen_num_splits", "fa_selftest_exp2", "attention_forward", "attention_forward_varlen",
+           "EXPORTED_SYMBOLS"]
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_noalloc", "fa_fwd_varlen", "fa_strerror", "fa_device_status",
-                    "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_varlen_num_splits")
+                    "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_varlen_num_splits",
+                    "fa_selftest_exp2")
 
 FA_OK = 0
 FA_ERR_DEVICE_TIMEOUT = -8
@@ -63,6 +65,8 @@ def load_library(path: str | None = None):
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_varlen_num_splits.argtypes = [i, i, i, i, i]
     lib.fa_varlen_num_splits.restype = i
+    lib.fa_selftest_exp2.argtypes = [vp, vp, vp, i, vp]
+    lib.fa_selftest_exp2.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -123,6 +127,13 @@ def fa_selftest_wait_timeout(limit_ns: int, stream: int | None = None) -> int:
     nothing completes until ``limit_ns`` passes, then records the timeout in
     the device status word. Returns the launch status."""
     return load_library().fa_selftest_wait_timeout(stream or None, limit_ns)
+
+
+def fa_selftest_exp2(x: int, y_approx: int, y_exp2f: int, n: int, stream: int | None = None) -> int:
+    """The C ``fa_selftest_exp2``: 2^x on the device by the softmax's
+    ex2.approx.ftz.f32 and by CUDA's exp2f, for n fp32 arguments (device
+    pointers as ints). Returns the status code."""
+    return load_library().fa_selftest_exp2(x, y_approx, y_exp2f, n, stream or None)
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,

@@ -53,7 +53,7 @@ def up_to_date() -> bool:
 # in the source assumes this many registers per thread at launch (384 threads
 # x 168). A different count would make setmaxnreg.inc wait for registers that
 # never come, so the build refuses it.
-LAUNCH_REGS = {"fa_fwd_ws_kernel": 168, "fa_fwd_varlen_kernel": 168}
+LAUNCH_REGS = {"fa_fwd_kernel": 168}
 
 
 def check_ptxas_report(report: str) -> dict[str, int]:

@@ -12,9 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "fa.h"
-#include "fa_fwd_ws.cuh"
-#include "fa_fwd_varlen.cuh"
-#include <cstdlib>
+#include "fa_fwd_kernel.cuh"
 
 namespace {
 
@@ -25,8 +23,9 @@ std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
 
-// Work-queue slots of the persistent kernel: {next unit, CTAs finished},
-// one 128-byte line each. A launch finds its slot zero and leaves it zero.
+// Work-queue slots of the persistent kernel: {next item, CTAs finished},
+// one 128-byte line each, in a fixed array of the library (zero when the
+// library is loaded; a launch finds its slot zero and leaves it zero).
 // Ordinary launches take the next of 64 slots in turn, so that many may be in
 // flight on different streams without sharing one. A launch captured into a
 // CUDA graph keeps the slot it drew at capture for every replay; it draws
@@ -36,33 +35,32 @@ unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
 constexpr int kSchedSlots = 64;
 constexpr int kGraphSlots = 192;
 constexpr int kSchedSlotWords = 32;
+static __device__ __align__(256) unsigned g_sched_ring[(kSchedSlots + kGraphSlots) * kSchedSlotWords];
+
+// Most CTAs that share out one unit's key tiles (the size of a portable
+// thread-block cluster).
+constexpr int kMaxClusterSplit = 8;
 
 struct DeviceState {
     bool probed = false;
     int status = FA_OK;  // FA_OK, FA_ERR_UNSUPPORTED_ARCH
     int sm_count = 0;
-    unsigned* sched = nullptr;  // (kSchedSlots + kGraphSlots) x kSchedSlotWords, allocated on first use
+    unsigned* sched = nullptr;  // device address of g_sched_ring on this device
     std::atomic<unsigned> sched_next{0};
     std::atomic<unsigned> graph_next{0};
-    cudaMemPool_t pool = nullptr;  // stream-ordered scratch for key-range splits
     std::atomic<bool> kernels_ready{false};  // shared-memory attributes of every kernel set
 };
 DeviceState g_devices[kMaxDevices];
 
-// Allocates and zeroes the device's work-queue ring once (the only device
-// allocation the library makes; it lives until the process exits).
+// Looks up the device address of the work-queue ring once per device (with
+// that device current). In host code the array's name is only a host-side
+// stand-in; the kernels must be given this address.
 int ensure_sched(DeviceState& st) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (st.sched) return FA_OK;
     void* ptr = nullptr;
-    const size_t bytes = sizeof(unsigned) * (kSchedSlots + kGraphSlots) * kSchedSlotWords;
-    if (cudaMalloc(&ptr, bytes) != cudaSuccess) {
+    if (cudaGetSymbolAddress(&ptr, g_sched_ring) != cudaSuccess || ptr == nullptr) {
         cudaGetLastError();
-        return FA_ERR_LAUNCH;
-    }
-    if (cudaMemset(ptr, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
-        cudaGetLastError();
-        cudaFree(ptr);
         return FA_ERR_LAUNCH;
     }
     st.sched = static_cast<unsigned*>(ptr);
@@ -113,72 +111,46 @@ int probe_device(int* dev_out, DeviceState** st_out) {
     return st.status;
 }
 
-// The device's pool for per-call split scratch: stream-ordered, so calls on
-// different streams never share it, and it keeps its memory between calls.
-int ensure_pool(int dev, DeviceState& st) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (st.pool) return FA_OK;
-    cudaMemPoolProps props{};
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    cudaMemPool_t pool = nullptr;
-    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
-        cudaGetLastError();
-        return FA_ERR_LAUNCH;
-    }
-    unsigned long long keep = ~0ull;
-    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    st.pool = pool;
-    return FA_OK;
+// Work items of an equal-length launch over `units` units of (head, 256
+// query rows) on `sms` SMs: every unit whole, except that a non-causal
+// problem whose last wave of whole units would fill at most half the SMs runs
+// those last units as two half items each (one 128-row tile, its key tiles
+// shared out between the two softmax warpgroups and merged inside the CTA),
+// so that wave takes half as long. A half item needs at least 4 key tiles,
+// and the units' second tiles must hold rows (so no half item lies wholly
+// past N).
+void plan_items(long long units, int N, int sms, bool causal, long long* n_full, long long* n_items) {
+    *n_full = units;
+    *n_items = units;
+    const long long nkt = (static_cast<long long>(N) + fa::kBlockN - 1) / fa::kBlockN;
+    const long long nqb = (static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+    if (causal || sms <= 0 || nkt < 4 || (2 * nqb - 1) * fa::kBlockM >= N) return;
+    const long long r = units % sms;
+    if (r == 0 || 2 * r > sms) return;
+    *n_full = units - r;
+    *n_items = units + r;
 }
 
-// Number of splits of each unit's key range: only without the causal mask
-// (whose units differ in size and balance through the work queue), only
-// while each split keeps at least 4 key tiles, and only when it raises the
-// share of busy CTA slots in the last wave by more than 3 points.
-int choose_nsplit(long long units, int n_k_tiles, int sms, bool causal) {
-    if (causal || sms <= 0) return 1;
-    auto eff = [&](long long items) {
-        const long long waves = (items + sms - 1) / sms;
-        return static_cast<double>(items) / static_cast<double>(waves * sms);
-    };
-    int best = 1;
-    double best_eff = eff(units);
-    for (int sp = 2; sp <= 4; ++sp) {
-        if (n_k_tiles / sp < 4) break;
-        const double e = eff(units * sp);
-        if (e > best_eff + 0.03) {
-            best = sp;
-            best_eff = e;
-        }
-    }
-    return best;
-}
-
-// Number of splits of each unit's key range in a variable-length batch.
-// Units are (sequence, head, 256-query block); with few of them (decode: one
-// query per sequence) most SMs would sit idle. One CTA streams K/V at about
-// 60 GB/s (measured on GB300, decode at d = 128), so about 0.6 x the SM count
-// of work items in flight reach the HBM limit, and every split beyond that
-// only adds its fixed cost (Q load, pipeline fill, partial write, merge).
-// The count is the fewest splits that give that many items, with at least 4
-// key tiles (by the mean key count per sequence) per split, 64 at most.
+// Number of CTAs that share out each unit's key range in a variable-length
+// batch (the cluster size of the launch). Units are (sequence, head,
+// 256-query block); with few of them (decode: one query per sequence) most
+// SMs would sit idle. One CTA streams K/V at about 60 GB/s (measured on
+// GB300, decode at d = 128), so about 0.6 x the SM count of CTAs at work
+// reach the HBM limit, and every split beyond that only adds its fixed cost
+// (Q load, pipeline fill, merge). The count is the fewest splits that give
+// that many items, with at least 4 key tiles (by the mean key count per
+// sequence) per split, 8 (a portable cluster) at most.
 int choose_nsplit_varlen(long long units, long long B, long long total_k, int sms) {
     const long long kt = (total_k / B + fa::kBlockN - 1) / fa::kBlockN;  // mean key tiles per sequence
     if (sms <= 0 || units <= 0 || kt < 8) return 1;
     const long long target = (6LL * sms + 9) / 10;
     if (units >= target) return 1;
     const long long want = (target + units - 1) / units;
-    return static_cast<int>(std::max<long long>(1, std::min<long long>({want, kt / 4, 64})));
+    return static_cast<int>(std::max<long long>(1, std::min<long long>({want, kt / 4, kMaxClusterSplit})));
 }
 
-// choose_nsplit_varlen, lowered until the unit counter holds every item plus
-// one over-claim per CTA.
 int varlen_splits(long long units, long long B, long long total_k, int sms) {
-    int sp = choose_nsplit_varlen(units, B, total_k, sms);
-    while (sp > 1 && units * sp > 0x7fffffffLL - 65536) --sp;
-    return sp;
+    return choose_nsplit_varlen(units, B, total_k, sms);
 }
 
 // 3-D view [B*H][N][d] of a contiguous bf16 [B,H,N,d] tensor, boxes of
@@ -217,25 +189,46 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 // Persistent warp-specialised kernel: one CTA per SM (its shared memory and
-// all 512 TMEM columns keep it alone on the SM), looping over work units of
-// one head x 256 query rows.
-template <int D, bool CAUSAL>
-int launch_ws(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-              const fa::FwdParams& prm, int dev, int sm_count, cudaStream_t stream) {
+// all 512 TMEM columns keep it alone on the SM), looping over work items. A
+// cluster split (variable length, prm.sched == null) runs one item per CTA,
+// the CTAs of a unit's shares forming one cluster.
+template <int D, bool CAUSAL, bool VARLEN>
+int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                  const fa::FwdParams& prm, int sm_count, cudaStream_t stream) {
     using Cfg = fa::WsCfg<D>;
-    auto kernel = fa::fa_fwd_ws_kernel<D, CAUSAL>;
-    (void)dev;
-    const long long nqb = (static_cast<long long>(prm.N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-    const long long items = nqb * prm.num_heads_total * (prm.nsplit > 1 ? prm.nsplit : 1);
-    const unsigned grid = static_cast<unsigned>(items < sm_count ? items : sm_count);
+    auto kernel = fa::fa_fwd_kernel<D, CAUSAL, VARLEN>;
+    if (prm.sched == nullptr) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(prm.n_items), 1, 1);
+        cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(prm.nsplit);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, prm) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_LAUNCH;
+        }
+        return FA_OK;
+    }
+    const unsigned grid = static_cast<unsigned>(prm.n_items < sm_count ? prm.n_items : sm_count);
     kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-template <int D, bool CAUSAL>
-int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-           const fa::FwdParams& prm, int dev, int sm_count, cudaStream_t stream) {
-    return launch_ws<D, CAUSAL>(tq, tk, tv, to, prm, dev, sm_count, stream);
+template <bool VARLEN>
+int launch_any(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& to, const fa::FwdParams& prm, int sms, cudaStream_t s) {
+    if (d == 64)
+        return causal ? launch_kernel<64, true, VARLEN>(tq, tk, tv, to, prm, sms, s)
+                      : launch_kernel<64, false, VARLEN>(tq, tk, tv, to, prm, sms, s);
+    return causal ? launch_kernel<128, true, VARLEN>(tq, tk, tv, to, prm, sms, s)
+                  : launch_kernel<128, false, VARLEN>(tq, tk, tv, to, prm, sms, s);
 }
 
 template <typename Kernel>
@@ -252,14 +245,14 @@ int prepare_kernels(DeviceState& st) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (st.kernels_ready.load(std::memory_order_relaxed)) return FA_OK;
     const int b64 = fa::WsCfg<64>::kSmemBytes, b128 = fa::WsCfg<128>::kSmemBytes;
-    const bool ok = set_smem_attr(fa::fa_fwd_ws_kernel<64, false>, b64) &&
-                    set_smem_attr(fa::fa_fwd_ws_kernel<64, true>, b64) &&
-                    set_smem_attr(fa::fa_fwd_ws_kernel<128, false>, b128) &&
-                    set_smem_attr(fa::fa_fwd_ws_kernel<128, true>, b128) &&
-                    set_smem_attr(fa::vl::fa_fwd_varlen_kernel<64, false>, b64) &&
-                    set_smem_attr(fa::vl::fa_fwd_varlen_kernel<64, true>, b64) &&
-                    set_smem_attr(fa::vl::fa_fwd_varlen_kernel<128, false>, b128) &&
-                    set_smem_attr(fa::vl::fa_fwd_varlen_kernel<128, true>, b128);
+    const bool ok = set_smem_attr(fa::fa_fwd_kernel<64, false, false>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<64, true, false>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, false, false>, b128) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, true, false>, b128) &&
+                    set_smem_attr(fa::fa_fwd_kernel<64, false, true>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<64, true, true>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, false, true>, b128) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, true, true>, b128);
     if (!ok) return FA_ERR_LAUNCH;
     st.kernels_ready.store(true, std::memory_order_release);
     return FA_OK;
@@ -277,26 +270,23 @@ int capturing(cudaStream_t stream) {
     return cs == cudaStreamCaptureStatusActive ? 1 : -1;
 }
 
-// The work-queue slot (and, on the first ordinary call, the device's launch
-// setup: kernel attributes, the slot ring, the split-scratch pool) of a
-// launch on `stream`. While the stream is captured nothing is allocated or
-// set: the device must have had an ordinary call before.
-int take_sched_slot(int dev, DeviceState& st, cudaStream_t stream, unsigned** slot) {
+// The device's launch setup (kernel attributes, the ring's address), made by
+// its first ordinary call; a call made while `stream` is being captured
+// needs it made already. *captured tells which of the two it was.
+int ready_for_launch(DeviceState& st, cudaStream_t stream, bool* captured) {
     const int cap = capturing(stream);
     if (cap < 0) return FA_ERR_LAUNCH;
-    if (cap == 0) {
-        if (prepare_kernels(st) != FA_OK || ensure_sched(st) != FA_OK || ensure_pool(dev, st) != FA_OK)
-            return FA_ERR_LAUNCH;
-        *slot = st.sched + (st.sched_next.fetch_add(1) % kSchedSlots) * kSchedSlotWords;
-        return FA_OK;
-    }
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!st.kernels_ready.load(std::memory_order_relaxed) || st.sched == nullptr || st.pool == nullptr)
-            return FA_ERR_LAUNCH;
-    }
-    *slot = st.sched + (kSchedSlots + st.graph_next.fetch_add(1) % kGraphSlots) * kSchedSlotWords;
-    return FA_OK;
+    *captured = cap == 1;
+    if (cap == 0) return (prepare_kernels(st) == FA_OK && ensure_sched(st) == FA_OK) ? FA_OK : FA_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(g_mu);
+    return (st.kernels_ready.load(std::memory_order_relaxed) && st.sched != nullptr) ? FA_OK : FA_ERR_LAUNCH;
+}
+
+// The work-queue slot of a launch (ordinary and captured launches draw from
+// separate parts of the ring).
+unsigned* take_sched_slot(DeviceState& st, bool captured) {
+    if (!captured) return st.sched + (st.sched_next.fetch_add(1) % kSchedSlots) * kSchedSlotWords;
+    return st.sched + (kSchedSlots + st.graph_next.fetch_add(1) % kGraphSlots) * kSchedSlotWords;
 }
 
 // One warp waits on an mbarrier phase that nothing completes, through the
@@ -314,19 +304,71 @@ __global__ void __launch_bounds__(32, 1) fa_selftest_timeout_kernel(unsigned lon
     fa::wait_phase_warp(fa::ptx::smem_u32(&bar), 0, &abort_flag, fa::kStatusTimeoutOther, limit_ns);
 }
 
-// The variable-length kernel: same launch shape, one unit per (sequence,
-// head, 256-query block) of the longest sequence.
-template <int D, bool CAUSAL>
-int launch_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                  const fa::vl::VlParams& prm, int dev, int sm_count, cudaStream_t stream) {
-    using Cfg = fa::WsCfg<D>;
-    auto kernel = fa::vl::fa_fwd_varlen_kernel<D, CAUSAL>;
-    (void)dev;
-    const long long nqb = (static_cast<long long>(prm.max_nq) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-    const long long items = nqb * prm.num_heads_total * prm.nsplit;
-    const unsigned grid = static_cast<unsigned>(items < sm_count ? items : sm_count);
-    kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, prm);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+// 2^x for n arguments, with the instruction the softmax uses
+// (ex2.approx.ftz.f32) and with CUDA's exp2f, so that a test can hold the
+// former to its error bound.
+__global__ void __launch_bounds__(256) fa_selftest_exp2_kernel(const float* x, float* y_approx, float* y_exp2f,
+                                                               int n) {
+    const int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
+    if (i < n) {
+        y_approx[i] = fa::ptx::ex2_approx(x[i]);
+        y_exp2f[i] = exp2f(x[i]);
+    }
+}
+
+// Host-side checks shared by the equal-length entry points: FA_OK, or the
+// code of the first violated rule. *units receives B*H*ceil(N/256).
+int check_dense(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                float scale, long long* units) {
+    if (!q || !k || !v || !o) return FA_ERR_NULL_PTR;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long nqb = (static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+    // work items (at most twice the units) plus one over-claim per CTA fit the int counter
+    if (BH > 0x7fffffffLL || 2 * BH * nqb > 0x7fffffffLL - 65536) return FA_ERR_BAD_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEAD_DIM;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_MISALIGNED;
+    const size_t tensor_bytes = static_cast<size_t>(BH) * N * d * 2;
+    const size_t lse_bytes = static_cast<size_t>(BH) * N * 4;
+    if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
+        overlaps(o, tensor_bytes, v, tensor_bytes))
+        return FA_ERR_ALIAS;
+    if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
+                overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, o, tensor_bytes)))
+        return FA_ERR_ALIAS;
+    *units = BH * nqb;
+    return FA_OK;
+}
+
+// Tensor maps, parameters and the launch of an equal-length forward pass
+// whose work-queue slot is `sched`.
+int run_dense(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+              float scale, int causal, long long units, unsigned* sched, int sms, cudaStream_t s) {
+    const int bh = B * H;
+    CUtensorMap tq, tk, tv, to;
+    if (encode_map(&tq, q, bh, N, d) != FA_OK || encode_map(&tk, k, bh, N, d) != FA_OK ||
+        encode_map(&tv, v, bh, N, d) != FA_OK || encode_map(&to, o, bh, N, d) != FA_OK)
+        return FA_ERR_LAUNCH;
+    fa::FwdParams prm{};
+    prm.lse = lse;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        prm.wait_limit_ns = g_wait_limit_ns;
+    }
+    prm.sched = sched;
+    prm.num_heads_total = bh;
+    prm.nqb = static_cast<int>((static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM));
+    prm.N = N;
+    long long n_full = units, n_items = units;
+    plan_items(units, N, sms, causal != 0, &n_full, &n_items);
+    prm.n_full = static_cast<int>(n_full);
+    prm.n_items = static_cast<int>(n_items);
+    prm.nsplit = 1;
+    return launch_any<false>(d, causal != 0, tq, tk, tv, to, prm, sms, s);
 }
 
 }  // namespace
@@ -342,6 +384,22 @@ int fa_selftest_wait_timeout(void* stream, unsigned long long limit_ns) {
     if (rc != FA_OK) return rc;
     if (limit_ns < 200000ull || limit_ns > 1000000000ull) return FA_ERR_BAD_SHAPE;
     fa_selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_selftest_exp2(const float* x, float* y_approx, float* y_exp2f, int n, void* stream) {
+    if (n < 0) return FA_ERR_BAD_SHAPE;
+    if (n == 0) return FA_OK;
+    if (!x || !y_approx || !y_exp2f) return FA_ERR_NULL_PTR;
+    if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y_approx) |
+          reinterpret_cast<uintptr_t>(y_exp2f)) & 3u) != 0)
+        return FA_ERR_MISALIGNED;
+    int dev = -1;
+    DeviceState* st = nullptr;
+    const int rc = probe_device(&dev, &st);
+    if (rc != FA_OK) return rc;
+    const unsigned blocks = static_cast<unsigned>((static_cast<long long>(n) + 255) / 256);
+    fa_selftest_exp2_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y_approx, y_exp2f, n);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -385,83 +443,18 @@ int fa_device_status(void* stream, unsigned* bits) {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, float scale,
            int causal, void* stream) {
-    if (!q || !k || !v || !o) return FA_ERR_NULL_PTR;
-    if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
-    const long long BH = static_cast<long long>(B) * H;
-    const long long n_q_tiles = (static_cast<long long>(N) + fa::kBlockM - 1) / fa::kBlockM;
-    if (BH > 0x7fffffffLL || BH * n_q_tiles > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEAD_DIM;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
-    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
-    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_MISALIGNED;
-    const size_t tensor_bytes = static_cast<size_t>(BH) * N * d * 2;
-    const size_t lse_bytes = static_cast<size_t>(BH) * N * 4;
-    if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
-        overlaps(o, tensor_bytes, v, tensor_bytes))
-        return FA_ERR_ALIAS;
-    if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
-                overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, o, tensor_bytes)))
-        return FA_ERR_ALIAS;
-
+    long long units = 0;
+    int rc = check_dense(q, k, v, o, lse, B, H, N, d, scale, &units);
+    if (rc != FA_OK) return rc;
     int dev = -1;
     DeviceState* st = nullptr;
-    int rc = probe_device(&dev, &st);
+    rc = probe_device(&dev, &st);
     if (rc != FA_OK) return rc;
-
-    CUtensorMap tq, tk, tv, to;
-    const int bh = static_cast<int>(BH);
-    if (encode_map(&tq, q, bh, N, d) != FA_OK || encode_map(&tk, k, bh, N, d) != FA_OK ||
-        encode_map(&tv, v, bh, N, d) != FA_OK || encode_map(&to, o, bh, N, d) != FA_OK)
-        return FA_ERR_LAUNCH;
-
-    fa::FwdParams prm{};
-    prm.lse = lse;
-    prm.N = N;
-    prm.num_heads_total = bh;
-    prm.num_q_tiles = static_cast<int>(n_q_tiles);
-    prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        prm.wait_limit_ns = g_wait_limit_ns;
-    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (take_sched_slot(dev, *st, s, &prm.sched) != FA_OK) return FA_ERR_LAUNCH;
-    const int sms = st->sm_count;
-    const long long units = ((static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM)) * BH;
-    const int n_k_tiles = static_cast<int>((static_cast<long long>(N) + fa::kBlockN - 1) / fa::kBlockN);
-    prm.nsplit = choose_nsplit(units, n_k_tiles, sms, causal != 0);
-    void* scratch = nullptr;
-    if (prm.nsplit > 1) {
-        // per call, stream-ordered: [partial O | partial LSE | tickets]
-        const size_t items = static_cast<size_t>(units) * prm.nsplit;
-        const size_t o_bytes = items * 2 * fa::kBlockM * d * sizeof(float);
-        const size_t l_bytes = items * 2 * fa::kBlockM * sizeof(float);
-        const size_t t_bytes = static_cast<size_t>(units) * 2 * sizeof(unsigned);
-        if (ensure_pool(dev, *st) != FA_OK ||
-            cudaMallocFromPoolAsync(&scratch, o_bytes + l_bytes + t_bytes, st->pool, s) != cudaSuccess) {
-            cudaGetLastError();
-            return FA_ERR_LAUNCH;
-        }
-        prm.part_o = static_cast<float*>(scratch);
-        prm.part_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
-        prm.tickets = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + o_bytes + l_bytes);
-        if (cudaMemsetAsync(prm.tickets, 0, t_bytes, s) != cudaSuccess) {
-            cudaGetLastError();
-            cudaFreeAsync(scratch, s);
-            return FA_ERR_LAUNCH;
-        }
-    }
-    if (d == 64)
-        rc = causal ? launch<64, true>(tq, tk, tv, to, prm, dev, sms, s) : launch<64, false>(tq, tk, tv, to, prm, dev, sms, s);
-    else
-        rc = causal ? launch<128, true>(tq, tk, tv, to, prm, dev, sms, s)
-                    : launch<128, false>(tq, tk, tv, to, prm, dev, sms, s);
-    if (scratch && cudaFreeAsync(scratch, s) != cudaSuccess) {
-        cudaGetLastError();
-        if (rc == FA_OK) rc = FA_ERR_LAUNCH;
-    }
-    return rc;
+    bool captured = false;
+    if (ready_for_launch(*st, s, &captured) != FA_OK) return FA_ERR_LAUNCH;
+    return run_dense(q, k, v, o, lse, B, H, N, d, scale, causal, units, take_sched_slot(*st, captured),
+                     st->sm_count, s);
 }
 
 int fa_varlen_num_splits(int B, int H, int total_k, int max_seqlen_q, int sm_count) {
@@ -513,62 +506,31 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
         encode_map_tokens(&tv, total_k ? v : q, total_k ? total_k : 1, H, d) != FA_OK)
         return FA_ERR_LAUNCH;
 
-    fa::vl::VlParams prm{};
-    prm.o = o;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool captured = false;
+    if (ready_for_launch(*st, s, &captured) != FA_OK) return FA_ERR_LAUNCH;
+    const int sms = st->sm_count;
+    const long long units = BH * nqb;
+    fa::FwdParams prm{};
     prm.lse = lse;
-    prm.cu_q = cu_seqlens_q;
-    prm.cu_k = cu_seqlens_k;
-    prm.heads = H;
-    prm.num_heads_total = static_cast<int>(BH);
-    prm.total_q = total_q;
-    prm.max_nq = max_seqlen_q;
     prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     {
         std::lock_guard<std::mutex> lock(g_mu);
         prm.wait_limit_ns = g_wait_limit_ns;
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (take_sched_slot(dev, *st, s, &prm.sched) != FA_OK) return FA_ERR_LAUNCH;
-    const int sms = st->sm_count;
-    const long long units = BH * nqb;
+    prm.num_heads_total = static_cast<int>(BH);
+    prm.nqb = static_cast<int>(nqb);
+    prm.o = o;
+    prm.cu_q = cu_seqlens_q;
+    prm.cu_k = cu_seqlens_k;
+    prm.heads = H;
+    prm.total_q = total_q;
     prm.nsplit = varlen_splits(units, B, total_k, sms);
-    void* scratch = nullptr;
-    if (prm.nsplit > 1) {
-        // per call, stream-ordered: [partial O | partial LSE | tickets], only
-        // for the query rows that can exist (max_seqlen_q of them per unit at most)
-        prm.part_tiles = max_seqlen_q > fa::kBlockM ? 2 : 1;
-        prm.part_rows = max_seqlen_q < fa::kBlockM ? max_seqlen_q : fa::kBlockM;
-        const size_t rows = static_cast<size_t>(units) * prm.nsplit * prm.part_tiles * prm.part_rows;
-        const size_t o_bytes = rows * d * sizeof(float);
-        const size_t l_bytes = rows * sizeof(float);
-        const size_t t_bytes = static_cast<size_t>(units) * 2 * sizeof(unsigned);
-        if (ensure_pool(dev, *st) != FA_OK ||
-            cudaMallocFromPoolAsync(&scratch, o_bytes + l_bytes + t_bytes, st->pool, s) != cudaSuccess) {
-            cudaGetLastError();
-            return FA_ERR_LAUNCH;
-        }
-        prm.part_o = static_cast<float*>(scratch);
-        prm.part_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
-        prm.tickets = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + o_bytes + l_bytes);
-        if (cudaMemsetAsync(prm.tickets, 0, t_bytes, s) != cudaSuccess) {
-            cudaGetLastError();
-            cudaFreeAsync(scratch, s);
-            return FA_ERR_LAUNCH;
-        }
-    } else {
-        prm.nsplit = 1;
-    }
-    if (d == 64)
-        rc = causal ? launch_varlen<64, true>(tq, tk, tv, prm, dev, sms, s)
-                    : launch_varlen<64, false>(tq, tk, tv, prm, dev, sms, s);
-    else
-        rc = causal ? launch_varlen<128, true>(tq, tk, tv, prm, dev, sms, s)
-                    : launch_varlen<128, false>(tq, tk, tv, prm, dev, sms, s);
-    if (scratch && cudaFreeAsync(scratch, s) != cudaSuccess) {
-        cudaGetLastError();
-        if (rc == FA_OK) rc = FA_ERR_LAUNCH;
-    }
-    return rc;
+    prm.n_items = static_cast<int>(units * prm.nsplit);
+    prm.n_full = prm.n_items;
+    // a cluster split runs one item per CTA and needs no work queue
+    prm.sched = prm.nsplit > 1 ? nullptr : take_sched_slot(*st, captured);
+    return launch_any<true>(d, causal != 0, tq, tk, tv, tq, prm, sms, s);
 }
 
 }  // extern "C"
@@ -576,19 +538,18 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
 // ---------------------------------------------------------------------------
 // Allocation-free entry point.
 //
-// fa_fwd keeps its work-queue counters in device memory that the library
-// allocates with cudaMalloc on the first call. Some callers cannot have any
-// allocation happen inside a library call: code running where cudaMalloc is
-// forbidden or would synchronise the device at the wrong moment (inside a
-// custom allocator or memory-pool callback, under a caller-side memory budget
-// that must account for every byte, or in a runtime that pre-plans all device
-// memory up front). fa_fwd_noalloc runs the same kernel with its scratch in
-// the fixed array below, which every GPU that loads the library holds until
-// the process exits. It never calls cudaMalloc, cudaFree or any allocating
-// routine.
+// Some callers cannot have a library call allocate device memory: code that
+// runs inside a custom allocator or memory-pool callback (where cudaMalloc
+// would re-enter the allocator or synchronise the device at the wrong
+// moment), a caller-side memory budget that must account for every byte, or
+// a runtime that plans all device memory before it starts. fa_fwd_noalloc is
+// the entry point with that promise in its contract: it runs the same kernel
+// as fa_fwd with its work-queue counters in the fixed array below, which
+// every GPU that loads the library holds until the process exits. It never
+// calls cudaMalloc, cudaFree or any allocating routine.
 namespace {
 
-// One work-queue slot {next unit, CTAs finished}, padded to a 128-byte line.
+// One work-queue slot {next item, CTAs finished}, padded to a 128-byte line.
 constexpr int kNoAllocScratchWords = 32;
 static __device__ __align__(256) unsigned g_noalloc_scratch[kNoAllocScratchWords];
 
@@ -615,72 +576,29 @@ int noalloc_scratch(int dev, unsigned** out) {
 
 extern "C" int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                               int N, int d, float scale, int causal, void* stream) {
-    if (!q || !k || !v || !o) return FA_ERR_NULL_PTR;
-    if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
-    const long long BH = static_cast<long long>(B) * H;
-    const long long n_q_tiles = (static_cast<long long>(N) + fa::kBlockM - 1) / fa::kBlockM;
-    if (BH > 0x7fffffffLL || BH * n_q_tiles > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
-    // The scratch is one fixed work-queue slot whatever the shape; what it
-    // limits is the unit counter, which must hold every unit plus one
-    // over-claim per CTA.
-    const long long units = ((static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM)) * BH;
-    if (units + 65536LL > 0xffffffffLL) return FA_ERR_BAD_SHAPE;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEAD_DIM;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
-    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
-    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_MISALIGNED;
-    const size_t tensor_bytes = static_cast<size_t>(BH) * N * d * 2;
-    const size_t lse_bytes = static_cast<size_t>(BH) * N * 4;
-    if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
-        overlaps(o, tensor_bytes, v, tensor_bytes))
-        return FA_ERR_ALIAS;
-    if (lse && (overlaps(lse, lse_bytes, q, tensor_bytes) || overlaps(lse, lse_bytes, k, tensor_bytes) ||
-                overlaps(lse, lse_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, o, tensor_bytes)))
-        return FA_ERR_ALIAS;
-
+    // The scratch is one fixed work-queue slot whatever the shape; the shape
+    // limits are fa_fwd's.
+    long long units = 0;
+    int rc = check_dense(q, k, v, o, lse, B, H, N, d, scale, &units);
+    if (rc != FA_OK) return rc;
     int dev = -1;
     DeviceState* st = nullptr;
-    int rc = probe_device(&dev, &st);
+    rc = probe_device(&dev, &st);
     if (rc != FA_OK) return rc;
     unsigned* scratch = nullptr;
     if (noalloc_scratch(dev, &scratch) != FA_OK) return FA_ERR_LAUNCH;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     {
         // kernel attributes are set by an ordinary call, never during a capture
-        const int cap = capturing(static_cast<cudaStream_t>(stream));
+        const int cap = capturing(s);
         if (cap < 0) return FA_ERR_LAUNCH;
         if (cap == 0 ? prepare_kernels(*st) != FA_OK : !st->kernels_ready.load(std::memory_order_acquire))
             return FA_ERR_LAUNCH;
     }
-
-    CUtensorMap tq, tk, tv, to;
-    const int bh = static_cast<int>(BH);
-    if (encode_map(&tq, q, bh, N, d) != FA_OK || encode_map(&tk, k, bh, N, d) != FA_OK ||
-        encode_map(&tv, v, bh, N, d) != FA_OK || encode_map(&to, o, bh, N, d) != FA_OK)
-        return FA_ERR_LAUNCH;
-
-    fa::FwdParams prm{};
-    prm.lse = lse;
-    prm.N = N;
-    prm.num_heads_total = bh;
-    prm.num_q_tiles = static_cast<int>(n_q_tiles);
-    prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        prm.wait_limit_ns = g_wait_limit_ns;
-    }
-    prm.sched = scratch;
-    prm.nsplit = 1;  // no key-range split: its partial results would need more scratch
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the two counters must start at zero (the kernel also leaves them zero)
     if (cudaMemsetAsync(scratch, 0, 2 * sizeof(unsigned), s) != cudaSuccess) {
         cudaGetLastError();
         return FA_ERR_LAUNCH;
     }
-    const int sms = st->sm_count;
-    if (d == 64)
-        return causal ? launch_ws<64, true>(tq, tk, tv, to, prm, dev, sms, s)
-                      : launch_ws<64, false>(tq, tk, tv, to, prm, dev, sms, s);
-    return causal ? launch_ws<128, true>(tq, tk, tv, to, prm, dev, sms, s)
-                  : launch_ws<128, false>(tq, tk, tv, to, prm, dev, sms, s);
+    return run_dense(q, k, v, o, lse, B, H, N, d, scale, causal, units, scratch, st->sm_count, s);
 }

@@ -28,21 +28,27 @@ enum : unsigned {
     kStatusTimeoutOther = 1u << 4,
 };
 
+// Parameters of one launch of the forward kernel. Equal-length batches use
+// N and n_full; variable-length batches the last group.
 struct FwdParams {
-    float* lse;           // [B*H, N] fp32, or null
-    int N;                // sequence length (queries = keys)
-    int num_heads_total;  // B*H
-    int num_q_tiles;      // ceil(N / 128)
+    float* lse;           // equal length: [B*H, N]; variable length: [H, total_q]; fp32, or null
     float scale_log2;     // scale * log2(e): scores are kept in base-2 units
     unsigned long long wait_limit_ns;  // give up on an mbarrier wait after this long
-    unsigned* sched;      // work-queue slot {next unit, CTAs finished}; zero at launch, zero again at exit
-    // Key-range split (non-causal problems with few work units): each unit's
-    // key tiles are divided among `nsplit` work items whose partial results
-    // are merged by the last one to finish. nsplit = 1: no scratch is used.
-    int nsplit;
-    float* part_o;        // [items][2 tiles][d/4][128 rows][4] fp32: normalised partial O
-    float* part_lse;      // [items][2 tiles][128 rows] fp32: base-2 log-sum-exp of each partial
-    unsigned* tickets;    // [units][2 tiles], zero at launch: splits of a tile finished so far
+    unsigned* sched;      // work-queue slot (next item, CTAs finished): zero at launch, zero again at
+                          // exit. Null: every CTA runs the one item blockIdx.x (a cluster split).
+    int num_heads_total;  // B*H
+    int nqb;              // 256-row query blocks per head (of the longest sequence, variable length)
+    int n_items;          // work items of the launch
+    // ---- equal length [B, H, N, d]
+    int N;                // sequence length (queries = keys)
+    int n_full;           // items [0, n_full) are whole units; every later unit runs as two half items
+    // ---- variable length [total, H, d]
+    void* o;              // [total_q, H, d] bf16 (plain stores: a TMA box would cross sequences)
+    const int* cu_q;      // [B + 1] query-token offsets
+    const int* cu_k;      // [B + 1] key-token offsets
+    int heads;            // H
+    int total_q;
+    int nsplit;           // CTAs of a cluster that share out each unit's key tiles (1: none)
 };
 
 // Device-wide status word (one per device that loads the library). Zero means

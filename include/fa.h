@@ -55,7 +55,8 @@ typedef enum fa_status {
  *          the natural-log log-sum-exp of each query row's scaled scores
  *          over the keys the row may see.
  * B, H, N  batch, heads, sequence length (queries = keys = N), each >= 1;
- *          B*H <= 2^31-1 and ceil(N/128)*B*H <= 2^31-1.
+ *          B*H <= 2^31-1 and 2*B*H*ceil(N/256) <= 2^31-1 - 65536 (work
+ *          items and one over-claim per CTA fit the int counter).
  * d        head dimension: 64 or 128.
  * scale    score scale (the pages use 1/sqrt(d)); finite and > 0.
  * causal   nonzero: key j is hidden from query i when j > i (top-left
@@ -63,39 +64,39 @@ typedef enum fa_status {
  * stream   cudaStream_t to run on, as void*; NULL = legacy default stream.
  *
  * Ownership: the caller allocates and owns every buffer; the library keeps
- * no pointer after the call returns. The library's own state is one 32 KB
- * device buffer per device (work-queue counters for the persistent kernel),
- * allocated and zeroed by the first fa_fwd or fa_fwd_varlen call on that
- * device (that first call synchronises the device) and kept until the
- * process exits. Each launch uses one of its 64 counter slots in turn and
- * leaves it zeroed, so up to 64 launches may be in flight at once on
- * different streams. A non-causal
- * problem with few work units per SM splits each unit's key range in 2-4
- * parts; such a call also takes a scratch buffer for the partial results
- * (about nsplit * B*H*N*(d+1)*4 bytes) from a stream-ordered memory pool that
- * the library creates per device, and frees it on `stream` after its kernel
- * (fa_fwd_noalloc never splits). The call is asynchronous: argument errors
- * are returned before anything is queued; faults inside the kernel appear at
- * the caller's next synchronisation, and a kernel that gave up on a wait
- * leaves its O/LSE rows unwritten and reports through fa_device_status().
- * The current device must be compute capability 10.3 (sm_103a).
+ * no pointer after the call returns and allocates no device memory, neither
+ * per call nor once: its only device state is a fixed 32 KB array inside the
+ * library (work-queue counters: 256 slots of 128 bytes) and the device status
+ * word, which every GPU that loads the library holds until the process exits.
+ * Per device it caches the SM count, the kernels' shared-memory attributes
+ * and that array's device address, all set by the first ordinary call of any
+ * forward entry point on that device (with the device current). Each launch
+ * uses one of 64 counter slots in turn and leaves it zeroed, so up to 64
+ * launches may be in flight at once on different streams. A non-causal
+ * problem whose last wave of work units would leave most SMs idle runs those
+ * units as half units (one 128-row query tile whose key tiles the CTA's two
+ * softmax warpgroups share out, merged inside the CTA): no scratch memory.
+ * The call is asynchronous: argument errors are returned before anything is
+ * queued; faults inside the kernel appear at the caller's next
+ * synchronisation, and a kernel that gave up on a wait leaves its O/LSE rows
+ * unwritten and reports through fa_device_status(). The current device must
+ * be compute capability 10.3 (sm_103a).
  *
  * CUDA graphs: fa_fwd, fa_fwd_varlen and fa_fwd_noalloc may be called while
  * `stream` is being captured (cudaStreamBeginCapture, torch.cuda.graph),
- * once the device has had one ordinary call of the same entry point: that
- * call allocates and sets what a capture may not (the counter buffer, the
- * scratch pool, the kernels' shared-memory sizes). A call captured before
- * then returns FA_ERR_LAUNCH and enqueues nothing. The tensor maps are
- * encoded from the pointers given at capture, so a replay reads and writes
- * those buffers, which must stay allocated while the graph may be replayed
- * (a replay after one was freed reads or writes unmapped or reused memory;
- * torch.cuda.graph returns the allocator's free blocks to the driver when a
- * capture begins). A captured call keeps the counter slot it drew for every
- * replay, from 192 slots that ordinary calls never use, so replays may
- * overlap ordinary launches and replays of other graphs on other streams
- * (until 192 calls have been captured on the device, when the slots wrap);
- * a key-range split's scratch becomes an allocation node of the graph.
- * fa_fwd_noalloc's one shared slot stays shared when captured.
+ * once the device has had one ordinary call of a forward entry point: that
+ * call sets what a capture may not (the kernels' shared-memory sizes, the
+ * counter array's address). A call captured before then returns
+ * FA_ERR_LAUNCH and enqueues nothing. The tensor maps are encoded from the
+ * pointers given at capture, so a replay reads and writes those buffers,
+ * which must stay allocated while the graph may be replayed (a replay after
+ * one was freed reads or writes unmapped or reused memory; torch.cuda.graph
+ * returns the allocator's free blocks to the driver when a capture begins). A
+ * captured call keeps the counter slot it drew for every replay, from 192
+ * slots that ordinary calls never use, so replays may overlap ordinary
+ * launches and replays of other graphs on other streams (until 192 calls have
+ * been captured on the device, when the slots wrap). fa_fwd_noalloc's one
+ * shared slot stays shared when captured.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, void* stream);
@@ -108,18 +109,18 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * before it starts. (The pages describe no such entry point; it is part of
  * this library's interface only.)
  *
- * Arguments, layouts, ownership and errors are those of fa_fwd. It never calls
- * cudaMalloc, cudaFree or any allocating routine: its scratch (one 128-byte
- * work-queue slot) is a fixed array inside the library that every GPU which
- * loads the library keeps until the process exits. The first call on a
- * device looks up that array's device address (with that device current);
- * make the first call before any stream capture. Each call clears the slot's
- * counters on `stream` before its kernel, and every call shares the one slot:
- * calls whose kernels overlap on the GPU (different streams, no ordering
- * between them) race on it and must not be issued. The scratch does not grow
- * with the problem; the one size it limits is the unit count
- * B*H*ceil(N/256), which must stay below 2^32 - 65536 (FA_ERR_BAD_SHAPE
- * otherwise; fa_fwd's own limits are stricter).
+ * Arguments, layouts, ownership, limits and errors are those of fa_fwd,
+ * and it gives fa_fwd's results bit for bit. It never calls cudaMalloc,
+ * cudaFree or any allocating routine (fa_fwd does not either; this entry
+ * point states it as its contract and keeps its own counters): its scratch
+ * (one 128-byte work-queue slot) is a fixed array inside the library that
+ * every GPU which loads the library keeps until the process exits. The
+ * first call on a device looks up that array's device address (with that
+ * device current); make the first call before any stream capture. Each call
+ * clears the slot's counters on `stream` before its kernel, and every call
+ * shares the one slot: calls whose kernels overlap on the GPU (different
+ * streams, no ordering between them) race on it and must not be issued. The
+ * scratch does not grow with the problem.
  */
 int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int H, int N, int d, float scale, int causal, void* stream);
@@ -157,23 +158,24 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
  *
  * Work is split into units of (sequence, head, 256 queries). When there are
  * few units for the GPU's SMs (decode: a few sequences of one query against
- * long key sets), each unit's key tiles are divided among several work items
- * (fa_varlen_num_splits gives how many). Each item writes its partial O,
- * normalised, and its LSE to scratch memory, and the last item of a unit to
- * finish merges them: O = sum_s 2^(L_s - L) O_s with L = log2 sum_s 2^L_s
- * (base-2 LSEs), the online-softmax rescaling applied across items. The
- * scratch memory comes, stream-ordered, from the same device memory pool as
- * fa_fwd's.
+ * long key sets), each unit's key tiles are shared out among the CTAs of a
+ * thread-block cluster (2-8 of them; fa_varlen_num_splits gives how many).
+ * Each CTA keeps its partial O, normalised, and its LSE in its own shared
+ * memory, and the cluster's first CTA merges them through distributed
+ * shared memory: O = sum_s 2^(L_s - L) O_s with L = log2 sum_s 2^L_s (base-2
+ * LSEs), the online-softmax rescaling applied across the shares. No device
+ * memory is allocated (fa_fwd's ownership rules apply).
  */
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                   const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H, int total_q,
                   int total_k, int max_seqlen_q, int d, float scale, int causal, void* stream);
 
 /*
- * fa_varlen_num_splits — host-only, no device call: how many work items
- * fa_fwd_varlen gives each unit's key range for these sizes on a GPU with
- * `sm_count` SMs (1 = no split). Returns FA_ERR_BAD_SHAPE under the same
- * shape rules as fa_fwd_varlen, or when sm_count < 1.
+ * fa_varlen_num_splits — host-only, no device call: among how many CTAs
+ * (a cluster) fa_fwd_varlen shares out each unit's key range for these sizes
+ * on a GPU with `sm_count` SMs (1 = no split, at most 8). Returns
+ * FA_ERR_BAD_SHAPE under the same shape rules as fa_fwd_varlen, or when
+ * sm_count < 1.
  */
 int fa_varlen_num_splits(int B, int H, int total_k, int max_seqlen_q, int sm_count);
 
@@ -209,6 +211,19 @@ void fa_set_wait_limit_ns(unsigned long long ns);
  * counterpart (they have no failure handling).
  */
 int fa_selftest_wait_timeout(void* stream, unsigned long long limit_ns);
+
+/*
+ * fa_selftest_exp2 — numerics self-test of the exponential. For i < n, writes
+ * y_approx[i] = 2^x[i] computed by the instruction the softmax uses
+ * (ex2.approx.ftz.f32: subnormal arguments and results flush to zero, 2^-inf
+ * = +0) and y_exp2f[i] = CUDA's exp2f(x[i]). x, y_approx, y_exp2f are device
+ * fp32 arrays of n elements, 4-byte aligned, owned by the caller; the call is
+ * asynchronous on `stream`. Returns FA_OK (also for n = 0), FA_ERR_BAD_SHAPE
+ * for n < 0, FA_ERR_NULL_PTR / FA_ERR_MISALIGNED for bad pointers, else the
+ * device and launch codes of fa_fwd. The pages have no counterpart (they call
+ * exp / expf without stating its accuracy).
+ */
+int fa_selftest_exp2(const float* x, float* y_approx, float* y_exp2f, int n, void* stream);
 
 /* ABI version of this header (bumped on any incompatible change). */
 int fa_abi_version(void);

@@ -1,4 +1,4 @@
-"""The build's register guard (CPU only). Both kernels split their registers
+"""The build's register guard (CPU only). The forward kernel splits its registers
 between warpgroups with setmaxnreg, assuming 168 registers per thread at
 launch (384 threads); a different allocation would leave a warpgroup waiting
 for registers that never come, so the build must refuse it. Also checks that
@@ -8,11 +8,11 @@ import pytest
 from exact_attention_91_gb300 import build as fb
 
 GOOD = """
-ptxas info    : Compiling entry function '_ZN2fa16fa_fwd_ws_kernelILi128ELb1EEEv14CUtensorMap_stS1_S1_S1_NS_9FwdParamsE' for 'sm_103a'
-ptxas info    : Function properties for _ZN2fa16fa_fwd_ws_kernelILi128ELb1EEEv14CUtensorMap_stS1_S1_S1_NS_9FwdParamsE
+ptxas info    : Compiling entry function '_ZN2fa13fa_fwd_kernelILi128ELb1ELb0EEEv14CUtensorMap_stS1_S1_S1_NS_9FwdParamsE' for 'sm_103a'
+ptxas info    : Function properties for _ZN2fa13fa_fwd_kernelILi128ELb1ELb0EEEv14CUtensorMap_stS1_S1_S1_NS_9FwdParamsE
     0 bytes stack frame, 0 bytes spill stores, 0 bytes spill loads
 ptxas info    : Used 168 registers, used 16 barriers
-ptxas info    : Compiling entry function '_ZN2fa2vl20fa_fwd_varlen_kernelILi64ELb0EEEv14CUtensorMap_stS2_S2_NS0_8VlParamsE' for 'sm_103a'
+ptxas info    : Compiling entry function '_ZN2fa13fa_fwd_kernelILi64ELb0ELb1EEEv14CUtensorMap_stS1_S1_S1_NS_9FwdParamsE' for 'sm_103a'
     0 bytes stack frame, 0 bytes spill stores, 0 bytes spill loads
 ptxas info    : Used 168 registers, used 16 barriers
 ptxas info    : Compiling entry function '_Z26fa_selftest_timeout_kernely' for 'sm_103a'
@@ -30,12 +30,12 @@ def test_a_different_register_count_is_refused():
         fb.check_ptxas_report(GOOD.replace("Used 168 registers", "Used 160 registers", 1))
 
 
-def test_a_report_without_one_of_the_kernels_is_refused():
-    only_dense = GOOD.split("ptxas info    : Compiling entry function '_ZN2fa2vl")[0]
-    with pytest.raises(RuntimeError, match="fa_fwd_varlen_kernel"):
-        fb.check_ptxas_report(only_dense)
+def test_a_report_without_the_kernel_is_refused():
+    only_selftest = GOOD.split("ptxas info    : Compiling entry function '_Z26")[1]
+    with pytest.raises(RuntimeError, match="fa_fwd_kernel"):
+        fb.check_ptxas_report("ptxas info    : Compiling entry function '_Z26" + only_selftest)
 
 
 def test_every_split_kernel_is_guarded():
-    assert set(fb.LAUNCH_REGS) == {"fa_fwd_ws_kernel", "fa_fwd_varlen_kernel"}
+    assert set(fb.LAUNCH_REGS) == {"fa_fwd_kernel"}
     assert all(v == 168 for v in fb.LAUNCH_REGS.values())

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 DENSE = [
     # (B, H, N, d, causal): a ragged causal case, a non-causal one with few
-    # units (its key range is split: pool allocation and memset nodes), d=128
+    # units (they run as half units), d=128
     (2, 4, 1000, 64, True),
     (1, 8, 4096, 64, False),
     (2, 2, 777, 128, False),
@@ -69,7 +69,7 @@ def test_captured_dense_call_matches_ordinary_call(case):
 def test_captured_varlen_and_noalloc_calls_match_ordinary_calls():
     torch = _torch()
     import exact_attention_91_gb300 as fa
-    # decode of two sequences against long key sets: a split key range
+    # decode of two sequences against long key sets: a cluster split
     x = fin.make_varlen_inputs([1, 3], [20000, 9000], 4, 128, seed=931)
     q, k, v = to_device(x.q), to_device(x.k), to_device(x.v)
     cu_q, cu_k = torch.from_numpy(x.cu_q).cuda(), torch.from_numpy(x.cu_k).cuda()
