@@ -16,8 +16,11 @@ bounded sample of query rows.
 ``--impl reference`` times the oracle instead (rank 0 only), on the same
 workload, over a bounded sample of rows per step.
 
-Multi-GPU (torchrun): each rank runs its own independent batch (seeded by
-rank); no collective touches the data path ("scaling": "weak").
+Multi-GPU (torchrun): by default each rank runs its own independent batch
+(seeded by rank: "scaling": "weak"); with ``--scaling strong`` the ranks
+share one problem, each computing a contiguous range of its B·H heads
+(``head_shards``). Either way no collective touches the data path: heads are
+independent.
 """
 from __future__ import annotations
 
@@ -172,6 +175,23 @@ def rank_workload(w: fin.Workload, rank: int, world: int) -> fin.Workload:
     return fin.Workload(w.name, w.B, w.H, w.N, w.d, w.causal, w.values, w.seed + 1000 * rank)
 
 
+def local_problem(w: fin.Workload, rank: int, world: int, scaling: str):
+    """This rank's inputs (bf16 bits [B_l, H_l, N, d]) and the job's flops per
+    step. Weak: the rank's own independently seeded batch of the workload's
+    shape; the job does world x the workload's flops. Strong: the rank's
+    contiguous range of the one workload's B·H heads (as [1, count, N, d]);
+    the job does the workload's flops once."""
+    from exact_attention_91_gb300 import head_shards
+    if scaling == "weak" or world == 1:
+        x = fin.make_inputs(rank_workload(w, rank, world))
+        return x, (x.q, x.k, x.v), w.B, w.H, w.flops * world
+    x = fin.make_inputs(w)
+    BH = w.B * w.H
+    start, n = head_shards(BH, world)[rank]
+    part = tuple(np.ascontiguousarray(a.reshape(BH, w.N, w.d)[start:start + n][None]) for a in (x.q, x.k, x.v))
+    return x, part, 1, n, w.flops
+
+
 def max_over_ranks(ms: float, world: int, device) -> float:
     """The slowest rank's time (every rank must call it)."""
     if world == 1:
@@ -188,8 +208,11 @@ def job_throughput(world: int, steps: int, flops_step: float, ms_total: float) -
     return world * steps * flops_step / (ms_total * 1e-3) / 1e12
 
 
-def exp_roofline(w: fin.Workload, launch_s: float, clocks: dict, sm_count: int) -> dict:
-    pairs = w.B * w.H * (w.N * (w.N + 1) // 2 if w.causal else w.N * w.N)
+def exp_roofline(w: fin.Workload, launch_s: float, clocks: dict, sm_count: int, heads: int | None = None) -> dict:
+    """One ex2 per (query, visible key) of the `heads` heads a launch covers
+    (all of the workload's by default) against the MUFU rate."""
+    heads = w.B * w.H if heads is None else heads
+    pairs = heads * (w.N * (w.N + 1) // 2 if w.causal else w.N * w.N)
     mhz = (clocks or {}).get("sm_mhz") or 2070.0
     peak = 32.0 * sm_count * mhz * 1e6
     achieved = pairs / launch_s
@@ -301,11 +324,16 @@ def run_reference(args, w: fin.Workload):
     return 0
 
 
-def workload_config(w: fin.Workload, world: int) -> dict:
+def workload_config(w: fin.Workload, world: int, scaling: str = "weak") -> dict:
     ws = 4 * w.B * w.H * w.N * w.d * 2
+    if world == 1:
+        par = "single GPU"
+    elif scaling == "strong":
+        par = f"one problem, B*H heads sharded x{world}"
+    else:
+        par = f"independent batches x{world}"
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-            "values": w.values, "scale": w.scale, "seed": w.seed,
-            "parallelism": f"independent batches x{world}" if world > 1 else "single GPU",
+            "values": w.values, "scale": w.scale, "seed": w.seed, "parallelism": par,
             "l2": ("inputs larger than L2" if ws > 2 * L2_BYTES else "L2 flushed between timed launches")}
 
 
@@ -324,16 +352,16 @@ def run_ours(args, w: fin.Workload):
     fa.load_library()
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
 
-    x = fin.make_inputs(rank_workload(w, rank, world))
+    x, (xq, xk, xv), B, H, job_flops = local_problem(w, rank, world, args.scaling)
+    N, d = w.N, w.d
 
     def up(a):
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
-    q, k, v = up(x.q), up(x.k), up(x.v)
+    q, k, v = up(xq), up(xk), up(xv)
     o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
-    B, H, N, d = w.B, w.H, w.N, w.d
 
     def launch():
         rc = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
@@ -410,9 +438,9 @@ def run_ours(args, w: fin.Workload):
     # Two device buffer sets let the host->device copy of step i+1 (one
     # stream) and the device->host read of step i (another) overlap the
     # kernel of step i (a third), as a serving loop over this API would.
-    hq = torch.from_numpy(x.q.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hk = torch.from_numpy(x.k.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hv = torch.from_numpy(x.v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hq = torch.from_numpy(xq.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(xk.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(xv.view(np.int16)).view(torch.bfloat16).pin_memory()
     ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
     hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     e2e_steps = max(1, min(args.steps, 20))
@@ -463,9 +491,10 @@ def run_ours(args, w: fin.Workload):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     sampler.stop()
 
-    flops_step = w.flops
-    value = job_throughput(world, args.steps, flops_step, step_total_ms)
-    e2e_value = job_throughput(world, e2e_steps, flops_step, e2e_ms)
+    flops_step = w.flops * B * H / (w.B * w.H)   # this rank's launch
+    hbm_local = w.hbm_bytes * B * H // (w.B * w.H)
+    value = job_throughput(1, args.steps, job_flops, step_total_ms)
+    e2e_value = job_throughput(1, e2e_steps, job_flops, e2e_ms)
     avg_launch_s = kernel_ms / args.steps * 1e-3
     # the roofline uses the median launch (robust to a launch that met a clock
     # change or another process's work); the mean is reported beside it
@@ -489,8 +518,8 @@ def run_ours(args, w: fin.Workload):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, world),
+        "scaling": args.scaling, "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, world, args.scaling),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
@@ -504,16 +533,16 @@ def run_ours(args, w: fin.Workload):
                            "overlap the kernel of step i (three streams); host->device runs at "
                            "~211 GB/s (a 1 GB pinned copy on GB300), which bounds this number"},
         "gpu_launches": args.steps,
-        "hbm": {"achieved_gbs": w.hbm_bytes / median_launch_s / 1e9,
+        "hbm": {"achieved_gbs": hbm_local / median_launch_s / 1e9,
                 "peak_gbs": float((peaks or {}).get("hbm_gbs", 6800.0)),
-                "frac": w.hbm_bytes / median_launch_s / 1e9 / float((peaks or {}).get("hbm_gbs", 6800.0)),
-                "bytes_per_launch": w.hbm_bytes,
+                "frac": hbm_local / median_launch_s / 1e9 / float((peaks or {}).get("hbm_gbs", 6800.0)),
+                "bytes_per_launch": hbm_local,
                 "note": "compulsory bytes (Q, K, V read, O and LSE written) over the kernel time"},
         "warm_l2_ms_per_step": warm_ms,
         # the second ceiling: one ex2 per (query, visible key); MUFU issues 32
         # ex2 per clock per SM on GB300 (a probe of back-to-back ex2 measured
         # ~29 per clock per SM), at the median SM clock of the timed region
-        "exp_roofline": exp_roofline(w, median_launch_s, clocks, sm_count),
+        "exp_roofline": exp_roofline(w, median_launch_s, clocks, sm_count, heads=B * H),
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -643,6 +672,8 @@ def main(argv=None):
                          "(for profiling small cases)")
     ap.add_argument("--varlen", choices=VARLEN_MIXES, default=None,
                     help="measure fa_fwd_varlen on a synthetic variable-length batch instead")
+    ap.add_argument("--scaling", choices=["weak", "strong"], default="weak",
+                    help="N > 1: weak = every rank its own batch; strong = the ranks share one problem's heads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)

@@ -18,7 +18,7 @@ from .build import LIB_PATH
 __all__ = ["FaError", "load_library", "fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
            "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_fwd_varlen",
            "fa_varlen_num_splits", "fa_selftest_exp2", "attention_forward", "attention_forward_varlen",
-           "EXPORTED_SYMBOLS"]
+           "head_shards", "attention_forward_heads", "EXPORTED_SYMBOLS"]
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_noalloc", "fa_fwd_varlen", "fa_strerror", "fa_device_status",
                     "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_varlen_num_splits",
@@ -205,3 +205,60 @@ def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: 
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_varlen")
     return (out, lse) if return_lse else out
+
+
+def head_shards(num_heads_total: int, world: int) -> list[tuple[int, int]]:
+    """Contiguous ranges (start, count) of the flattened B*H head axis for
+    ``world`` ranks, in rank order, sizes differing by at most one (the first
+    ``num_heads_total % world`` ranks take one more). Heads are independent
+    (each head's O and LSE depend only on its own Q, K, V), so a rank that
+    holds its range's Q, K, V computes its O and LSE alone: the head-sharded
+    multi-GPU forward needs no exchange between ranks."""
+    if num_heads_total < 0 or world < 1:
+        raise ValueError("need num_heads_total >= 0 and world >= 1")
+    base, extra = divmod(num_heads_total, world)
+    out, start = [], 0
+    for r in range(world):
+        n = base + (1 if r < extra else 0)
+        out.append((start, n))
+        start += n
+    return out
+
+
+def attention_forward_heads(q, k, v, head_start: int, head_count: int, causal: bool = False,
+                            scale: float | None = None, out=None, lse=None, stream=None):
+    """fa_fwd on heads [head_start, head_start + head_count) of the flattened
+    B*H axis of contiguous bf16 CUDA tensors [B, H, N, d]: the C call gets
+    pointers into q, k, v (and into ``out`` / ``lse``, allocated whole when
+    not given), nothing is copied, and the other heads of ``out`` and ``lse``
+    are left as they were. Returns (out, lse) for the whole [B, H, N, d] /
+    [B, H, N] shape. Each rank of a head-sharded job calls this on the range
+    ``head_shards(B*H, world)[rank]`` of tensors in its own device memory."""
+    import torch
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k, v must be bf16")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [B, H, N, d]")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, H, N, d = q.shape
+    if head_start < 0 or head_count < 0 or head_start + head_count > B * H:
+        raise ValueError("head range outside [0, B*H)")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if head_count == 0:
+        return out, lse
+    eo, el = N * d * q.element_size(), N * 4   # bytes per head of q/k/v/out and of lse
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = fa_fwd(q.data_ptr() + head_start * eo, k.data_ptr() + head_start * eo, v.data_ptr() + head_start * eo,
+                out.data_ptr() + head_start * eo, lse.data_ptr() + head_start * el, 1, head_count, N, d,
+                float(scale), causal, s.cuda_stream)
+    if rc != FA_OK:
+        raise FaError(rc)
+    return out, lse

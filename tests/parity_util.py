@@ -4,12 +4,14 @@ CUDA path through the C ABI, and compare with the fp64 oracle.
 Tolerances (bf16 inputs and output, fp32 accumulation): O max |Δ| ≤ 1e-2 and
 mean |Δ| ≤ 1e-3 over the compared elements; LSE max |Δ| ≤ 1e-3.
 
-For shapes with very few keys per query (N = 2, say) each O row is an average
-of one or two V rows, so |O| is O(1) and the bf16 rounding of the exact O by
-itself costs close to 1e-3 on average (and up to a bf16 half-ulp of |O| ≈ 2-3,
-about 8e-3, at worst). Those extra shapes are held to the bars on top of that
-rounding floor (``rounding_floor=True``); the named workloads are held to the
-plain bars.
+A query row that sees at most FEW_KEYS keys (N ≤ 8, or the first rows under
+the causal mask) is an average of a handful of V rows, so |O| is O(1) and the
+bf16 rounding of the exact O alone costs up to half a bf16 ulp of |O| (7.8e-3
+at |O| in [2, 4)) and about 1e-3 on average. For those rows alone the max bar
+is 1e-2 on top of the half-ulp of each exact element, and the mean bar holds
+for the distance to the exact O rounded to bf16 (the result the output type
+can hold). Every other row is held to the plain bars against the fp64
+oracle.
 """
 from __future__ import annotations
 
@@ -47,17 +49,42 @@ def run_gpu(x: fin.Inputs, *, causal: bool | None = None, scale: float | None = 
     return o, lse
 
 
+FEW_KEYS = 8
+
+
+def visible_keys(N: int, causal: bool, i: np.ndarray) -> np.ndarray:
+    """Keys that query row i (0-based within its head) sees."""
+    i = np.asarray(i)
+    return (i + 1) if causal else np.full(i.shape, N)
+
+
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |x| (8 significant bits): the most
+    that rounding x to bf16 can cost."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(ax)) - 8.0)
+
+
 def compare(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray,
-            label: str = "") -> dict:
-    d_o = np.abs(o_gpu - o_ref)
+            label: str = "", keys: np.ndarray | None = None) -> dict:
+    """Error statistics of GPU O/LSE against the oracle. ``keys`` (shaped like
+    the LSE) gives each row's visible key count; rows with at most FEW_KEYS
+    keys get the rounding allowance described above."""
+    few = np.zeros(lse_ref.shape, bool) if keys is None else (np.asarray(keys) <= FEW_KEYS)
+    many = ~few
+    d_exact = np.abs(o_gpu - o_ref)
     d_l = np.abs(lse_gpu.astype(np.float64) - lse_ref)
-    # split of the O error: what bf16 rounding of the exact O alone costs
     o_ref_bf16 = fin.bf16_to_f64(fin.bf16_from_f64(o_ref))
     stats = {
-        "o_max_abs": float(d_o.max()),
-        "o_mean_abs": float(d_o.mean()),
+        # rows that see more than FEW_KEYS keys: the plain bars against the fp64 oracle
+        "o_max_abs": float(d_exact[many].max()) if many.any() else 0.0,
+        "o_mean_abs": float(d_exact[many].mean()) if many.any() else 0.0,
+        # rows that see at most FEW_KEYS keys
+        "few_key_rows": int(few.sum()),
+        "few_max_over_allowance": float((d_exact[few] - half_ulp_bf16(o_ref[few])).max()) if few.any() else 0.0,
+        "few_mean_vs_rounded": float(np.abs(o_gpu[few] - o_ref_bf16[few]).mean()) if few.any() else 0.0,
+        # what bf16 rounding of the exact O alone costs (for the record)
         "o_mean_abs_rounding_only": float(np.abs(o_ref_bf16 - o_ref).mean()),
-        "o_max_abs_rounding_only": float(np.abs(o_ref_bf16 - o_ref).max()),
         "lse_max_abs": float(d_l.max()),
         "finite": bool(np.isfinite(o_gpu).all() and np.isfinite(lse_gpu).all()),
     }
@@ -65,12 +92,12 @@ def compare(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: 
     return stats
 
 
-def assert_within(stats: dict, rounding_floor: bool = False) -> None:
+def assert_within(stats: dict) -> None:
     assert stats["finite"], stats
-    max_bar = O_MAX_ABS + (stats["o_max_abs_rounding_only"] if rounding_floor else 0.0)
-    assert stats["o_max_abs"] <= max_bar, stats
-    mean_bar = O_MEAN_ABS + (stats["o_mean_abs_rounding_only"] if rounding_floor else 0.0)
-    assert stats["o_mean_abs"] <= mean_bar, stats
+    assert stats["o_max_abs"] <= O_MAX_ABS, stats
+    assert stats["o_mean_abs"] <= O_MEAN_ABS, stats
+    assert stats["few_max_over_allowance"] <= O_MAX_ABS, stats
+    assert stats["few_mean_vs_rounded"] <= O_MEAN_ABS, stats
     assert stats["lse_max_abs"] <= LSE_MAX_ABS, stats
 
 

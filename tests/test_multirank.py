@@ -5,6 +5,7 @@ The reference arm runs on rank 0 only."""
 import os
 import socket
 
+import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")
@@ -105,3 +106,21 @@ def test_traffic_is_reported_only_for_the_captured_kernel(monkeypatch, tmp_path)
     assert bench.load_traffic("max_shift") is None          # never captured
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "missing.json"))
     assert bench.load_traffic("llm_prefill") is None
+
+
+def test_strong_scaling_ranks_share_one_problem_by_heads():
+    """--scaling strong: the ranks' head ranges cover the one workload's
+    heads once, their inputs are those heads' slices of its inputs, and the
+    job counts the workload's flops once per step (weak: once per rank)."""
+    w = fin.custom(2, 3, 64, 64, True, seed=11)
+    x = fin.make_inputs(w)
+    BH = w.B * w.H
+    got = []
+    for rank in range(4):
+        _, (q, k, v), B, H, job = bench.local_problem(w, rank, 4, "strong")
+        assert B == 1 and q.shape == (1, H, w.N, w.d) and job == w.flops
+        got.append(q[0])
+    assert np.array_equal(np.concatenate(got), x.q.reshape(BH, w.N, w.d))
+    _, (q, _, _), B, H, job = bench.local_problem(w, 1, 4, "weak")
+    assert (B, H) == (w.B, w.H) and job == 4 * w.flops and not np.array_equal(q, x.q)
+    assert bench.workload_config(w, 4, "strong")["parallelism"].startswith("one problem")
