@@ -188,16 +188,18 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-// Persistent warp-specialised kernel: one CTA per SM (its shared memory and
-// all 512 TMEM columns keep it alone on the SM), looping over work items. A
-// cluster split (variable length, prm.sched == null) runs one item per CTA,
-// the CTAs of a unit's shares forming one cluster.
+// Warp-specialised kernel: one CTA per SM (its shared memory and all 512
+// TMEM columns keep it alone on the SM). With a work-queue slot the grid is
+// persistent (min(items, SMs) CTAs loop over the items); without one
+// (prm.sched == null: no more items than SMs, or a cluster split) every CTA
+// runs the one item blockIdx.x, the CTAs of a unit's shares forming one
+// cluster when nsplit > 1.
 template <int D, bool CAUSAL, bool VARLEN>
 int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                   const fa::FwdParams& prm, int sm_count, cudaStream_t stream) {
     using Cfg = fa::WsCfg<D>;
     auto kernel = fa::fa_fwd_kernel<D, CAUSAL, VARLEN>;
-    if (prm.sched == nullptr) {
+    if (prm.nsplit > 1) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(static_cast<unsigned>(prm.n_items), 1, 1);
         cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
@@ -216,7 +218,8 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
         }
         return FA_OK;
     }
-    const unsigned grid = static_cast<unsigned>(prm.n_items < sm_count ? prm.n_items : sm_count);
+    const unsigned grid =
+        static_cast<unsigned>(prm.sched == nullptr || prm.n_items < sm_count ? prm.n_items : sm_count);
     kernel<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -368,6 +371,8 @@ int run_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
     prm.n_full = static_cast<int>(n_full);
     prm.n_items = static_cast<int>(n_items);
     prm.nsplit = 1;
+    // no more items than SMs: one item per CTA, no work queue to claim from or reset
+    if (n_items <= sms) prm.sched = nullptr;
     return launch_any<false>(d, causal != 0, tq, tk, tv, to, prm, sms, s);
 }
 
@@ -528,8 +533,8 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
     prm.nsplit = varlen_splits(units, B, total_k, sms);
     prm.n_items = static_cast<int>(units * prm.nsplit);
     prm.n_full = prm.n_items;
-    // a cluster split runs one item per CTA and needs no work queue
-    prm.sched = prm.nsplit > 1 ? nullptr : take_sched_slot(*st, captured);
+    // a cluster split, or no more items than SMs: one item per CTA, no work queue
+    prm.sched = (prm.nsplit > 1 || prm.n_items <= sms) ? nullptr : take_sched_slot(*st, captured);
     return launch_any<true>(d, causal != 0, tq, tk, tv, tq, prm, sms, s);
 }
 

@@ -102,7 +102,10 @@ struct WsCfg {
     // Named barriers: 1 + t for softmax warpgroup t; the two softmax
     // warpgroups together (half-item merge, cluster-split hand-over); all 12
     // warps (setup and teardown).
-    static constexpr uint32_t kBarPair = 3, kBarPairDone = 4, kBarAll = 15;
+    // kBarSetup: the TMA warp only arrives (it starts its first copies while
+    // TMEM is allocated), every other warp waits; a barrier of its own, so
+    // that a TMA warp that finishes early cannot count toward it at teardown.
+    static constexpr uint32_t kBarPair = 3, kBarPairDone = 4, kBarSetup = 14, kBarAll = 15;
     // The partial results of a cluster split (after the last MMA of the item,
     // when the ring is idle): fp32 O rows [tile][row][D] in the ring, base-2
     // LSE [tile][row] and the CTA's abort flag in the staging area.
@@ -984,13 +987,17 @@ __global__ void __launch_bounds__(384, 1)
             *sm.s_issued(1) = 0u;
             ptx::fence_mbar_init();
         }
-        ptx::tc_fence_before_sync();
-        ptx::named_bar_sync(Cfg::kBarAll, Cfg::kThreads);
-        ptx::tc_fence_after_sync();
         if (warp == 9) {
+            // the barriers and flags this warp uses are its own: it hands them
+            // over and starts loading at once
+            __syncwarp();
+            ptx::named_bar_arrive(Cfg::kBarSetup, Cfg::kThreads);
             load_role<D, CAUSAL, VARLEN>(tm_q, tm_k, tm_v, p, lane);
             __syncwarp();
         } else {
+            ptx::tc_fence_before_sync();
+            ptx::named_bar_sync(Cfg::kBarSetup, Cfg::kThreads);
+            ptx::tc_fence_after_sync();
             // warp 8: every S; warps 10 and 11: P·V of tile 0 and tile 1
             const int m = warp == 8 ? 0 : warp - 9;
             if (warp == 8)
@@ -1024,7 +1031,7 @@ __global__ void __launch_bounds__(384, 1)
     } else {
         ptx::regs_inc<kRegsSoftmax>();
         ptx::tc_fence_before_sync();
-        ptx::named_bar_sync(Cfg::kBarAll, Cfg::kThreads);
+        ptx::named_bar_sync(Cfg::kBarSetup, Cfg::kThreads);
         ptx::tc_fence_after_sync();
         softmax_role<D, CAUSAL, VARLEN>(tm_o, p, warp, lane);
         ptx::tc_fence_before_sync();
