@@ -112,19 +112,29 @@ int probe_device(int* dev_out, DeviceState** st_out) {
 }
 
 // Work items of an equal-length launch over `units` units of (head, 256
-// query rows) on `sms` SMs: every unit whole, except that a non-causal
-// problem whose last wave of whole units would fill at most half the SMs runs
-// those last units as two half items each (one 128-row tile, its key tiles
-// shared out between the two softmax warpgroups and merged inside the CTA),
-// so that wave takes half as long. A half item needs at least 4 key tiles,
-// and the units' second tiles must hold rows (so no half item lies wholly
-// past N).
+// query rows) on `sms` SMs: every unit whole, except:
+//  * a non-causal problem whose last wave of whole units would fill at most
+//    half the SMs runs those last units as two half items each (one 128-row
+//    tile, its key tiles shared out between the two softmax warpgroups and
+//    merged inside the CTA), so that wave takes half as long;
+//  * a causal problem with at most half as many units as SMs runs every unit
+//    as two half items, so that the longest chain of key tiles (a unit's
+//    last tile) is shared by two warpgroups.
+// A half item needs at least 4 key tiles (non-causal) or 2 (causal), and the
+// units' second tiles must hold rows (so no half item lies wholly past N).
 void plan_items(long long units, int N, int sms, bool causal, long long* n_full, long long* n_items) {
     *n_full = units;
     *n_items = units;
     const long long nkt = (static_cast<long long>(N) + fa::kBlockN - 1) / fa::kBlockN;
     const long long nqb = (static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-    if (causal || sms <= 0 || nkt < 4 || (2 * nqb - 1) * fa::kBlockM >= N) return;
+    if (sms <= 0 || (2 * nqb - 1) * fa::kBlockM >= N) return;
+    if (causal) {
+        if (nkt < 2 || 2 * units > sms) return;
+        *n_full = 0;
+        *n_items = 2 * units;
+        return;
+    }
+    if (nkt < 4) return;
     const long long r = units % sms;
     if (r == 0 || 2 * r > sms) return;
     *n_full = units - r;

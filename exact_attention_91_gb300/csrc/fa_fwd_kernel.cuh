@@ -241,11 +241,13 @@ __device__ __forceinline__ Item item_coords(int u, const FwdParams& p) {
             w.n1 = kv_tiles<CAUSAL>(2 * qb + 1, p.N, p.N);  // 0: tile 1 lies past the end of the head
             w.n_load = max(w.n0, w.n1);
         } else {
-            // (non-causal problems only: every key tile is visible to every row)
+            // the tile's visible key tiles (all of them without the causal mask),
+            // the even ones to tile 0's warpgroup and the odd ones to tile 1's
+            const int nv = kv_tiles<CAUSAL>(2 * qb + ht, p.N, p.N);
             w.qr0 = w.qr1 = (2 * qb + ht) * kBlockM;
-            w.n0 = (nkt + 1) >> 1;
-            w.n1 = nkt >> 1;
-            w.n_load = nkt;
+            w.n0 = (nv + 1) >> 1;
+            w.n1 = nv >> 1;
+            w.n_load = nv;
         }
     } else {
         const int unit = p.nsplit == 1 ? u : u / p.nsplit;
@@ -794,8 +796,11 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap& tm_o, const FwdP
                 continue;
             } else {
                 // merge the two halves: weights 2^(m_h - m) / (sum of 2^(m_h - m) l_h)
-                const float m1 = reinterpret_cast<const float*>(sm.stage(1))[2 * row];
-                const float l1 = reinterpret_cast<const float*>(sm.stage(1))[2 * row + 1];
+                // (a half whose tile sees a single key tile leaves tile 1's
+                // warpgroup without keys: m1 = -inf, l1 = 0, and O_1 is not read)
+                const bool has1 = w.n1 > 0;
+                const float m1 = has1 ? reinterpret_cast<const float*>(sm.stage(1))[2 * row] : -INFINITY;
+                const float l1 = has1 ? reinterpret_cast<const float*>(sm.stage(1))[2 * row + 1] : 0.f;
                 const float mx = fmaxf(m_ref, m1);
                 const float mu = (mx == -INFINITY) ? 0.f : mx;
                 const float a0 = ptx::ex2_approx(m_ref - mu), a1 = ptx::ex2_approx(m1 - mu);
@@ -807,12 +812,15 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap& tm_o, const FwdP
 #pragma unroll 1
                 for (int b = 0; b < D / kBoxCols; ++b) {
                     float o[64];
-                    {
+                    load_row64(tO + b * 64, o);
+                    if (has1) {
                         float o1[64];
-                        load_row64(tO + b * 64, o);
                         load_row64(tO1 + b * 64, o1);
 #pragma unroll
                         for (int e = 0; e < 64; ++e) o[e] = fmaf(w0, o[e], w1 * o1[e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) o[e] *= w0;
                     }
                     if (b == D / kBoxCols - 1) {
                         // every read of O_1 has landed: tile 1's warpgroup may go on
@@ -970,8 +978,9 @@ __global__ void __launch_bounds__(384, 1)
             ptx::tmem_alloc(ptx::smem_u32(sm.tmem_slot()), Cfg::kTmemCols);
             ptx::tmem_relinquish();
         }
-        if (warp == 9 && lane == 0) {
-            for (int i = 0; i < Cfg::kNumBars; ++i) {
+        if (warp == 9) {
+            // lane i initialises barriers i, i + 32, ...
+            for (int i = lane; i < Cfg::kNumBars; i += 32) {
                 const uint32_t b = sm.bar(i);
                 uint32_t count = 1;
                 if (b == sm.p_full(0) || b == sm.p_full(1) || b == sm.s_free(0) || b == sm.s_free(1))
@@ -982,9 +991,11 @@ __global__ void __launch_bounds__(384, 1)
                     if (b == sm.u_empty(q)) count = Cfg::kUnitConsumers;
                 ptx::mbar_init(b, count);
             }
-            *sm.abort_flag() = 0;
-            *sm.s_issued(0) = 0u;
-            *sm.s_issued(1) = 0u;
+            if (lane == 0) {
+                *sm.abort_flag() = 0;
+                *sm.s_issued(0) = 0u;
+                *sm.s_issued(1) = 0u;
+            }
             ptx::fence_mbar_init();
         }
         if (warp == 9) {

@@ -75,7 +75,9 @@ typedef enum fa_status {
  * launches may be in flight at once on different streams. A non-causal
  * problem whose last wave of work units would leave most SMs idle runs those
  * units as half units (one 128-row query tile whose key tiles the CTA's two
- * softmax warpgroups share out, merged inside the CTA): no scratch memory.
+ * softmax warpgroups share out, merged inside the CTA), and so does every
+ * unit of a causal problem with at most half as many units as SMs: no
+ * scratch memory.
  * The call is asynchronous: argument errors are returned before anything is
  * queued; faults inside the kernel appear at the caller's next
  * synchronisation, and a kernel that gave up on a wait leaves its O/LSE rows
