@@ -204,11 +204,11 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // (prm.sched == null: no more items than SMs, or a cluster split) every CTA
 // runs the one item blockIdx.x, the CTAs of a unit's shares forming one
 // cluster when nsplit > 1.
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool HALF>
 int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                   const fa::FwdParams& prm, int sm_count, cudaStream_t stream) {
     using Cfg = fa::WsCfg<D>;
-    auto kernel = fa::fa_fwd_kernel<D, CAUSAL, VARLEN>;
+    auto kernel = fa::fa_fwd_kernel<D, CAUSAL, VARLEN, HALF>;
     if (prm.nsplit > 1) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(static_cast<unsigned>(prm.n_items), 1, 1);
@@ -234,14 +234,16 @@ int launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-template <bool VARLEN>
+// HALF: the launch has half items (prm.n_items > prm.n_full; equal length only)
+template <bool VARLEN, bool HALF>
 int launch_any(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& to, const fa::FwdParams& prm, int sms, cudaStream_t s) {
+    static_assert(!(VARLEN && HALF), "half items are equal-length only");
     if (d == 64)
-        return causal ? launch_kernel<64, true, VARLEN>(tq, tk, tv, to, prm, sms, s)
-                      : launch_kernel<64, false, VARLEN>(tq, tk, tv, to, prm, sms, s);
-    return causal ? launch_kernel<128, true, VARLEN>(tq, tk, tv, to, prm, sms, s)
-                  : launch_kernel<128, false, VARLEN>(tq, tk, tv, to, prm, sms, s);
+        return causal ? launch_kernel<64, true, VARLEN, HALF>(tq, tk, tv, to, prm, sms, s)
+                      : launch_kernel<64, false, VARLEN, HALF>(tq, tk, tv, to, prm, sms, s);
+    return causal ? launch_kernel<128, true, VARLEN, HALF>(tq, tk, tv, to, prm, sms, s)
+                  : launch_kernel<128, false, VARLEN, HALF>(tq, tk, tv, to, prm, sms, s);
 }
 
 template <typename Kernel>
@@ -258,14 +260,19 @@ int prepare_kernels(DeviceState& st) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (st.kernels_ready.load(std::memory_order_relaxed)) return FA_OK;
     const int b64 = fa::WsCfg<64>::kSmemBytes, b128 = fa::WsCfg<128>::kSmemBytes;
-    const bool ok = set_smem_attr(fa::fa_fwd_kernel<64, false, false>, b64) &&
-                    set_smem_attr(fa::fa_fwd_kernel<64, true, false>, b64) &&
-                    set_smem_attr(fa::fa_fwd_kernel<128, false, false>, b128) &&
-                    set_smem_attr(fa::fa_fwd_kernel<128, true, false>, b128) &&
-                    set_smem_attr(fa::fa_fwd_kernel<64, false, true>, b64) &&
-                    set_smem_attr(fa::fa_fwd_kernel<64, true, true>, b64) &&
-                    set_smem_attr(fa::fa_fwd_kernel<128, false, true>, b128) &&
-                    set_smem_attr(fa::fa_fwd_kernel<128, true, true>, b128);
+    // <D, CAUSAL, VARLEN, HALF>
+    const bool ok = set_smem_attr(fa::fa_fwd_kernel<64, false, false, false>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<64, true, false, false>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, false, false, false>, b128) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, true, false, false>, b128) &&
+                    set_smem_attr(fa::fa_fwd_kernel<64, false, false, true>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<64, true, false, true>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, false, false, true>, b128) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, true, false, true>, b128) &&
+                    set_smem_attr(fa::fa_fwd_kernel<64, false, true, false>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<64, true, true, false>, b64) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, false, true, false>, b128) &&
+                    set_smem_attr(fa::fa_fwd_kernel<128, true, true, false>, b128);
     if (!ok) return FA_ERR_LAUNCH;
     st.kernels_ready.store(true, std::memory_order_release);
     return FA_OK;
@@ -383,7 +390,8 @@ int run_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
     prm.nsplit = 1;
     // no more items than SMs: one item per CTA, no work queue to claim from or reset
     if (n_items <= sms) prm.sched = nullptr;
-    return launch_any<false>(d, causal != 0, tq, tk, tv, to, prm, sms, s);
+    return n_items > n_full ? launch_any<false, true>(d, causal != 0, tq, tk, tv, to, prm, sms, s)
+                            : launch_any<false, false>(d, causal != 0, tq, tk, tv, to, prm, sms, s);
 }
 
 }  // namespace
@@ -545,7 +553,7 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
     prm.n_full = prm.n_items;
     // a cluster split, or no more items than SMs: one item per CTA, no work queue
     prm.sched = (prm.nsplit > 1 || prm.n_items <= sms) ? nullptr : take_sched_slot(*st, captured);
-    return launch_any<true>(d, causal != 0, tq, tk, tv, tq, prm, sms, s);
+    return launch_any<true, false>(d, causal != 0, tq, tk, tv, tq, prm, sms, s);
 }
 
 }  // extern "C"

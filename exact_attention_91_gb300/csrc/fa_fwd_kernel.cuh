@@ -8,11 +8,14 @@
 // share every K/V tile the CTA streams through shared memory. The tensor core
 // alternates between the two tiles, so the softmax of one tile runs while the
 // MMAs of the other are in flight. A work item is a whole unit, or:
-//   * (equal length, non-causal) a half unit: one 128-row tile whose key
-//     tiles the two softmax warpgroups share out (even ones to tile 0, odd
-//     ones to tile 1); their results are merged inside the CTA at the end.
-//     The last units of a launch run this way when a last wave of whole
-//     units would leave most SMs idle.
+//   * (equal length) a half unit: one 128-row tile whose key tiles the two
+//     softmax warpgroups share out (even ones to tile 0, odd ones to tile
+//     1); their results are merged inside the CTA at the end. The last units
+//     of a non-causal launch run this way when a last wave of whole units
+//     would leave most SMs idle, and every unit of a causal launch with at
+//     most half as many units as SMs. Only the instantiation with HALF set
+//     holds this code: carried unused, its branches cost the d = 128 kernel
+//     3-5% of its throughput.
 //   * (variable length, few units) one share of a unit's key tiles; the
 //     shares of a unit run on the CTAs of one thread-block cluster and are
 //     merged through distributed shared memory.
@@ -216,14 +219,14 @@ struct Item {
     __device__ __forceinline__ int key_tile(int t, int i) const { return half ? 2 * i + t : jb + i; }
 };
 
-template <bool CAUSAL, bool VARLEN>
+template <bool CAUSAL, bool VARLEN, bool HALF>
 __device__ __forceinline__ Item item_coords(int u, const FwdParams& p) {
     Item w;
     w.jb = 0;
     int qb;
     if constexpr (!VARLEN) {
         int unit = u, ht = 0;
-        w.half = u >= p.n_full;
+        w.half = HALF && u >= p.n_full;
         if (w.half) {
             const int h = u - p.n_full;
             unit = p.n_full + (h >> 1);
@@ -233,7 +236,6 @@ __device__ __forceinline__ Item item_coords(int u, const FwdParams& p) {
         w.head = 0;
         w.tq0 = w.tk0 = 0;
         w.nq = w.nk = p.N;
-        const int nkt = (p.N + kBlockN - 1) / kBlockN;
         if (!w.half) {
             w.qr0 = qb * 2 * kBlockM;
             w.qr1 = w.qr0 + kBlockM;
@@ -305,7 +307,7 @@ __device__ __forceinline__ int claim_item(const FwdParams& p, int it) {
         if (it > 0) return -1;
         const int u = static_cast<int>(blockIdx.x);
         if constexpr (VARLEN) {
-            const Item c = item_coords<CAUSAL, VARLEN>(u, p);
+            const Item c = item_coords<CAUSAL, VARLEN, false>(u, p);
             if (c.qr0 >= c.nq) return -1;
         }
         return u;
@@ -314,7 +316,7 @@ __device__ __forceinline__ int claim_item(const FwdParams& p, int it) {
         const int u = static_cast<int>(atomicAdd(p.sched, 1u));
         if (u >= p.n_items) return -1;
         if constexpr (!VARLEN) return u;
-        const Item c = item_coords<CAUSAL, VARLEN>(u, p);
+        const Item c = item_coords<CAUSAL, VARLEN, false>(u, p);
         if (c.qr0 < c.nq) return u;
     }
 }
@@ -344,7 +346,7 @@ __device__ __forceinline__ void k_coords(const Item& w, int row, int& y, int& z)
 // ---------------------------------------------------------------- TMA producer
 // Run by the whole warp: addresses and coordinates stay warp-uniform and one
 // elected lane issues each copy.
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool HALF>
 __device__ __forceinline__ void load_role(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                           const CUtensorMap& tm_v, const FwdParams& p, int lane) {
     using Cfg = WsCfg<D>;
@@ -375,7 +377,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap& tm_q, const CUtenso
         }
         u = __shfl_sync(0xffffffffu, u, 0);
         if (u < 0) break;
-        const Item w = item_coords<CAUSAL, VARLEN>(u, p);
+        const Item w = item_coords<CAUSAL, VARLEN, HALF>(u, p);
         for (int t = 0; t < 2 && ok; ++t) {
             ok = wait_phase_warp(sm.q_empty(t), (it & 1) ^ 1, abort_flag, kStatusTimeoutFree, lim);
             if (!ok) break;
@@ -421,7 +423,7 @@ __device__ __forceinline__ void load_role(const CUtensorMap& tm_q, const CUtenso
 // everything written there before; with d = 128 both tiles share one buffer,
 // so S1 follows the read of S0 and the next S0 the read of S1. K slots are
 // released here.
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool HALF>
 __device__ __forceinline__ void s_role(const FwdParams& p, int lane) {
     using Cfg = WsCfg<D>;
     constexpr int S = Cfg::kStages;
@@ -468,7 +470,7 @@ __device__ __forceinline__ void s_role(const FwdParams& p, int lane) {
     for (int it = 0; ok; ++it) {
         const int u = next_unit(sm, it, lane, p);
         if (u < 0) break;
-        const Item w = item_coords<CAUSAL, VARLEN>(u, p);
+        const Item w = item_coords<CAUSAL, VARLEN, HALF>(u, p);
         if (!wait_phase_warp(sm.q_full(0), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
         if (!wait_phase_warp(sm.q_full(1), it & 1, abort_flag, kStatusTimeoutLoad, lim)) break;
         // a tile that sees no key still hands its Q buffer back
@@ -495,7 +497,7 @@ __device__ __forceinline__ void s_role(const FwdParams& p, int lane) {
 // rescale O_t. V slots are released by both P·V warps (two arrivals); the
 // ring steps tile t does not use are released without use, after their load,
 // so that the arrival lands in the slot's current use.
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool HALF>
 __device__ __forceinline__ void pv_role(const FwdParams& p, int lane, int t) {
     using Cfg = WsCfg<D>;
     constexpr int S = Cfg::kStages;
@@ -523,7 +525,7 @@ __device__ __forceinline__ void pv_role(const FwdParams& p, int lane, int t) {
     for (int it = 0; ok; ++it) {
         const int u = next_unit(sm, it, lane, p);
         if (u < 0) break;
-        const Item w = item_coords<CAUSAL, VARLEN>(u, p);
+        const Item w = item_coords<CAUSAL, VARLEN, HALF>(u, p);
         const int n_t = w.n(t);
         if (n_t == 0) ptx::mma_commit_elect(sm.o_full(t));  // nothing to add: O is all zero
         for (int j = 0; j < w.n_load; ++j) {
@@ -586,7 +588,7 @@ __device__ __forceinline__ void pack_row64(const float (&f)[64], Store&& store) 
 }
 
 // ---------------------------------------------------------------- softmax + epilogue
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool HALF>
 __device__ __forceinline__ void softmax_role(const CUtensorMap& tm_o, const FwdParams& p, int warp, int lane) {
     using Cfg = WsCfg<D>;
     constexpr float kTau = 32.0f;
@@ -610,7 +612,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap& tm_o, const FwdP
         const int u = next_unit(sm, it, lane, p);
         if (u == -2) failed = true;
         if (named_bar_or(1 + t, 128, u < 0)) break;  // the warpgroup agrees on stopping
-        const Item w = item_coords<CAUSAL, VARLEN>(u, p);
+        const Item w = item_coords<CAUSAL, VARLEN, HALF>(u, p);
         const int qr = w.qr(t);  // first query row of this tile within its sequence
         const int n_t = w.n(t);
         float m_ref = -INFINITY;  // reference max (base 2) that O and l are relative to
@@ -628,9 +630,10 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap& tm_o, const FwdP
             float mx0, mx1, mx2, mx3;
             const int key0 = w.key_tile(t, i) * kBlockN;  // first key of this tile within the sequence
             // key j is visible to query q when j < nk and (causal) j <= q + nk - nq
-            const bool need_mask = key0 + kBlockN > w.nk || (CAUSAL && key0 + kBlockN - 1 > qr + w.nk - w.nq);
-            int last = w.nk - 1 - key0;  // last visible column of this tile
-            if (CAUSAL) last = min(last, qr + row + w.nk - w.nq - key0);
+            const int nk = VARLEN ? w.nk : p.N, off = VARLEN ? w.nk - w.nq : 0;
+            const bool need_mask = key0 + kBlockN > nk || (CAUSAL && key0 + kBlockN - 1 > qr + off);
+            int last = nk - 1 - key0;  // last visible column of this tile
+            if (CAUSAL && need_mask) last = min(last, qr + row + off - key0);
             {
                 uint32_t r0[32], r1[32], r2[32], r3[32];
                 ptx::tmem_ld_32x32b_x32(tS + 0, r0);
@@ -898,7 +901,7 @@ __device__ __forceinline__ void cluster_merge(const FwdParams& p, int warp, int 
     int aborted = 0;
     for (int s = 0; s < ns; ++s) aborted |= ptx::ld_dsmem_s32(ptx::mapa_shared(ptx::smem_u32(sm.part_abort()), s));
     if (aborted) return;  // a share gave up on a wait (the status word says so): no output
-    const Item w = item_coords<CAUSAL, true>(static_cast<int>(blockIdx.x), p);
+    const Item w = item_coords<CAUSAL, true, false>(static_cast<int>(blockIdx.x), p);
     const int q = w.qr(t) + row;
     if (w.qr0 >= w.nq || q >= w.nq || w.tq0 + q < 0 || w.tq0 + q >= p.total_q) return;
     const uint32_t lse_addr = ptx::smem_u32(sm.part_lse(t, row));
@@ -957,7 +960,7 @@ __device__ __forceinline__ void cluster_merge(const FwdParams& p, int warp, int 
 // The forward kernel. Equal length: tm_q/k/v/o are (d, N, B*H) views of
 // [B, H, N, d]. Variable length: tm_q/k/v are (d, H, total) views of
 // [total, H, d] and tm_o is unused (O is written with plain stores).
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool HALF>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -1003,7 +1006,7 @@ __global__ void __launch_bounds__(384, 1)
             // over and starts loading at once
             __syncwarp();
             ptx::named_bar_arrive(Cfg::kBarSetup, Cfg::kThreads);
-            load_role<D, CAUSAL, VARLEN>(tm_q, tm_k, tm_v, p, lane);
+            load_role<D, CAUSAL, VARLEN, HALF>(tm_q, tm_k, tm_v, p, lane);
             __syncwarp();
         } else {
             ptx::tc_fence_before_sync();
@@ -1012,9 +1015,9 @@ __global__ void __launch_bounds__(384, 1)
             // warp 8: every S; warps 10 and 11: P·V of tile 0 and tile 1
             const int m = warp == 8 ? 0 : warp - 9;
             if (warp == 8)
-                s_role<D, CAUSAL, VARLEN>(p, lane);
+                s_role<D, CAUSAL, VARLEN, HALF>(p, lane);
             else
-                pv_role<D, CAUSAL, VARLEN>(p, lane, warp - 10);
+                pv_role<D, CAUSAL, VARLEN, HALF>(p, lane, warp - 10);
             __syncwarp();
             // every MMA this warp issued is done before TMEM can be freed
             if (lane == 0) {
@@ -1044,7 +1047,7 @@ __global__ void __launch_bounds__(384, 1)
         ptx::tc_fence_before_sync();
         ptx::named_bar_sync(Cfg::kBarSetup, Cfg::kThreads);
         ptx::tc_fence_after_sync();
-        softmax_role<D, CAUSAL, VARLEN>(tm_o, p, warp, lane);
+        softmax_role<D, CAUSAL, VARLEN, HALF>(tm_o, p, warp, lane);
         ptx::tc_fence_before_sync();
         ptx::named_bar_sync(Cfg::kBarAll, Cfg::kThreads);
         if (VARLEN && p.nsplit > 1 && threadIdx.x == 0) {
