@@ -21,6 +21,12 @@
  * Plain C types only: device pointers are `const void*` / `void*`, the CUDA
  * stream is passed as `void*` (a cudaStream_t; NULL is the legacy default
  * stream).
+ *
+ * Every forward kernel allows programmatic dependent launch: a kernel that the
+ * caller launches next on the same stream with programmatic stream
+ * serialization may start before the forward kernel has finished, and must
+ * call cudaGridDependencySynchronize (griddepcontrol.wait) before it reads O
+ * or LSE. Launches without that attribute keep plain stream order.
  */
 #ifndef FA_H_
 #define FA_H_
