@@ -208,16 +208,39 @@ def job_throughput(world: int, steps: int, flops_step: float, ms_total: float) -
     return world * steps * flops_step / (ms_total * 1e-3) / 1e12
 
 
-def exp_roofline(w: fin.Workload, launch_s: float, clocks: dict, sm_count: int, heads: int | None = None) -> dict:
+def exp_roofline(w: fin.Workload, launch_s: float, clocks: dict, sm_count: int, heads: int | None = None,
+                 ex2_per_clk: float | None = None) -> dict:
     """One ex2 per (query, visible key) of the `heads` heads a launch covers
-    (all of the workload's by default) against the MUFU rate."""
+    (all of the workload's by default) against the MUFU rate: the measured
+    ex2 per SM clock (`measure_ex2_rate`) when given, else the nominal 32."""
     heads = w.B * w.H if heads is None else heads
     pairs = heads * (w.N * (w.N + 1) // 2 if w.causal else w.N * w.N)
     mhz = (clocks or {}).get("sm_mhz") or 2070.0
-    peak = 32.0 * sm_count * mhz * 1e6
+    rate = ex2_per_clk if ex2_per_clk else 32.0
+    peak = rate * sm_count * mhz * 1e6
     achieved = pairs / launch_s
+    basis = (f"measured {rate:.1f} ex2/clk/SM (fa_selftest_ex2_rate, median over the SMs)" if ex2_per_clk
+             else "nominal 32 ex2/clk/SM")
     return {"achieved_per_s": achieved, "peak_per_s": peak, "frac": achieved / peak,
-            "exps_per_launch": pairs, "peak_basis": f"32 ex2/clk/SM x {sm_count} SMs x {mhz:.0f} MHz"}
+            "exps_per_launch": pairs, "peak_basis": f"{basis} x {sm_count} SMs x {mhz:.0f} MHz"}
+
+
+def measure_ex2_rate(fa, torch, dev, sm_count: int, iters: int = 2048):
+    """Exponentials per SM clock that the exponential unit sustains: one
+    block of back-to-back independent ex2.approx chains per SM, each block
+    timed in SM clocks by the library's probe; the median over the blocks.
+    None if the probe fails."""
+    cycles = torch.zeros(sm_count, dtype=torch.int64, device=dev)
+    sink = torch.empty(sm_count * fa.EX2_RATE_THREADS, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    for n in (64, iters):  # the first launch warms the code and the clocks
+        if fa.fa_selftest_ex2_rate(cycles.data_ptr(), sink.data_ptr(), sm_count, n, s) != 0:
+            return None
+    torch.cuda.synchronize(dev)
+    c = cycles.cpu().numpy().astype(np.float64)
+    if not (c > 0).all():
+        return None
+    return float(np.median(fa.EX2_RATE_THREADS * fa.EX2_RATE_CHAINS * iters / c))
 
 
 def cpu_model() -> str:
@@ -351,6 +374,7 @@ def run_ours(args, w: fin.Workload):
     dev = torch.device("cuda", local)
     fa.load_library()
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    ex2_rate = measure_ex2_rate(fa, torch, dev, sm_count)
 
     x, (xq, xk, xv), B, H, job_flops = local_problem(w, rank, world, args.scaling)
     N, d = w.N, w.d
@@ -539,10 +563,10 @@ def run_ours(args, w: fin.Workload):
                 "bytes_per_launch": hbm_local,
                 "note": "compulsory bytes (Q, K, V read, O and LSE written) over the kernel time"},
         "warm_l2_ms_per_step": warm_ms,
-        # the second ceiling: one ex2 per (query, visible key); MUFU issues 32
-        # ex2 per clock per SM on GB300 (a probe of back-to-back ex2 measured
-        # ~29 per clock per SM), at the median SM clock of the timed region
-        "exp_roofline": exp_roofline(w, median_launch_s, clocks, sm_count, heads=B * H),
+        # the second ceiling: one ex2 per (query, visible key) against the
+        # measured ex2 rate per SM clock, at the median SM clock of the timed
+        # region
+        "exp_roofline": exp_roofline(w, median_launch_s, clocks, sm_count, heads=B * H, ex2_per_clk=ex2_rate),
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

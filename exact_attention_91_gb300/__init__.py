@@ -17,12 +17,13 @@ from .build import LIB_PATH
 
 __all__ = ["FaError", "load_library", "fa_fwd", "fa_fwd_noalloc", "fa_strerror", "fa_device_status",
            "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_fwd_varlen",
-           "fa_varlen_num_splits", "fa_selftest_exp2", "attention_forward", "attention_forward_varlen",
+           "fa_varlen_num_splits", "fa_selftest_exp2", "fa_selftest_ex2_rate", "EX2_RATE_THREADS",
+           "EX2_RATE_CHAINS", "attention_forward", "attention_forward_varlen",
            "head_shards", "attention_forward_heads", "EXPORTED_SYMBOLS"]
 
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_noalloc", "fa_fwd_varlen", "fa_strerror", "fa_device_status",
                     "fa_set_wait_limit_ns", "fa_abi_version", "fa_selftest_wait_timeout", "fa_varlen_num_splits",
-                    "fa_selftest_exp2")
+                    "fa_selftest_exp2", "fa_selftest_ex2_rate")
 
 FA_OK = 0
 FA_ERR_DEVICE_TIMEOUT = -8
@@ -67,6 +68,8 @@ def load_library(path: str | None = None):
     lib.fa_varlen_num_splits.restype = i
     lib.fa_selftest_exp2.argtypes = [vp, vp, vp, i, vp]
     lib.fa_selftest_exp2.restype = i
+    lib.fa_selftest_ex2_rate.argtypes = [vp, vp, i, i, vp]
+    lib.fa_selftest_ex2_rate.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -134,6 +137,20 @@ def fa_selftest_exp2(x: int, y_approx: int, y_exp2f: int, n: int, stream: int | 
     ex2.approx.ftz.f32 and by CUDA's exp2f, for n fp32 arguments (device
     pointers as ints). Returns the status code."""
     return load_library().fa_selftest_exp2(x, y_approx, y_exp2f, n, stream or None)
+
+
+# fa_selftest_ex2_rate: threads per block and chains per thread
+EX2_RATE_THREADS = 1024
+EX2_RATE_CHAINS = 8
+
+
+def fa_selftest_ex2_rate(cycles: int, sink: int, blocks: int, iters: int, stream: int | None = None) -> int:
+    """The C ``fa_selftest_ex2_rate``: ``blocks`` blocks (one per SM) each
+    run EX2_RATE_THREADS x EX2_RATE_CHAINS chains of ``iters`` dependent
+    ex2.approx; ``cycles`` (device int64 [blocks]) receives each block's span
+    in SM clocks, ``sink`` (device fp32 [blocks * EX2_RATE_THREADS]) the
+    chains' last values. Returns the status code."""
+    return load_library().fa_selftest_ex2_rate(cycles, sink, blocks, iters, stream or None)
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,

@@ -336,6 +336,32 @@ __global__ void __launch_bounds__(256) fa_selftest_exp2_kernel(const float* x, f
     }
 }
 
+// Throughput probe of the exponential unit. Each of the block's 1024
+// threads runs 8 independent chains of `iters` dependent
+// ex2.approx.ftz.f32 (x <- -2^x, which stays in [-1, -0.5]); thread 0 records
+// the block's clock64 span between two block barriers. The requested dynamic
+// shared memory keeps one block per SM, so ex2 per SM clock = 8192 * iters /
+// cycles[b].
+constexpr int kEx2RateThreads = 1024, kEx2RateChains = 8, kEx2RateSmem = 120 * 1024;
+__global__ void __launch_bounds__(1024) fa_selftest_ex2_rate_kernel(long long* cycles, float* sink, int iters) {
+    float x[kEx2RateChains];
+#pragma unroll
+    for (int c = 0; c < kEx2RateChains; ++c) x[c] = -0.5f - 0.0625f * static_cast<float>(c);
+    __syncthreads();
+    const long long t0 = clock64();
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int c = 0; c < kEx2RateChains; ++c) x[c] = -fa::ptx::ex2_approx(x[c]);
+    }
+    __syncthreads();
+    const long long t1 = clock64();
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < kEx2RateChains; ++c) acc += x[c];
+    sink[static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x] = acc;
+    if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
 // Host-side checks shared by the equal-length entry points: FA_OK, or the
 // code of the first violated rule. *units receives B*H*ceil(N/256).
 int check_dense(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -423,6 +449,25 @@ int fa_selftest_exp2(const float* x, float* y_approx, float* y_exp2f, int n, voi
     if (rc != FA_OK) return rc;
     const unsigned blocks = static_cast<unsigned>((static_cast<long long>(n) + 255) / 256);
     fa_selftest_exp2_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y_approx, y_exp2f, n);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_selftest_ex2_rate(long long* cycles, float* sink, int blocks, int iters, void* stream) {
+    if (blocks < 1 || blocks > 4096 || iters < 1 || iters > (1 << 20)) return FA_ERR_BAD_SHAPE;
+    if (!cycles || !sink) return FA_ERR_NULL_PTR;
+    if ((reinterpret_cast<uintptr_t>(cycles) & 7u) != 0 || (reinterpret_cast<uintptr_t>(sink) & 3u) != 0)
+        return FA_ERR_MISALIGNED;
+    int dev = -1;
+    DeviceState* st = nullptr;
+    const int rc = probe_device(&dev, &st);
+    if (rc != FA_OK) return rc;
+    if (cudaFuncSetAttribute(fa_selftest_ex2_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kEx2RateSmem) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_LAUNCH;
+    }
+    fa_selftest_ex2_rate_kernel<<<static_cast<unsigned>(blocks), kEx2RateThreads, kEx2RateSmem,
+                                  static_cast<cudaStream_t>(stream)>>>(cycles, sink, iters);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -233,6 +233,22 @@ int fa_selftest_wait_timeout(void* stream, unsigned long long limit_ns);
  */
 int fa_selftest_exp2(const float* x, float* y_approx, float* y_exp2f, int n, void* stream);
 
+/*
+ * fa_selftest_ex2_rate — throughput probe of the exponential unit, the
+ * softmax's second ceiling beside the tensor cores (one ex2 per query and
+ * visible key). Launches `blocks` blocks of 1024 threads, one per SM (each
+ * asks for 120 KB of shared memory); every thread runs 8 independent chains
+ * of `iters` dependent ex2.approx.ftz.f32. cycles (device, int64 [blocks],
+ * 8-byte aligned) receives each block's span in SM clocks; sink (device,
+ * fp32 [blocks * 1024], 4-byte aligned) receives the chains' final values so
+ * that no work is elided. The rate is 8192 * iters / cycles[b] ex2 per clock
+ * of block b's SM. Asynchronous on `stream`. Returns FA_OK once launched,
+ * FA_ERR_BAD_SHAPE unless 1 <= blocks <= 4096 and 1 <= iters <= 2^20,
+ * FA_ERR_NULL_PTR / FA_ERR_MISALIGNED for bad pointers, else the device and
+ * launch codes of fa_fwd. The pages have no counterpart.
+ */
+int fa_selftest_ex2_rate(long long* cycles, float* sink, int blocks, int iters, void* stream);
+
 /* ABI version of this header (bumped on any incompatible change). */
 int fa_abi_version(void);
 
