@@ -197,3 +197,29 @@ def test_scale_argument(fa_lib, oracle_mod):
     x = fin.make_inputs(fin.custom(1, 2, 300, 64, True, seed=35))
     _full_check(oracle_mod, x, scale=0.05)
     _full_check(oracle_mod, x, scale=1.0 / math.sqrt(64) * 2.0)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_whole_and_half_units_in_one_launch(fa_lib, oracle_mod, d):
+    """A non-causal launch with a few more units than SMs runs most units
+    whole and its last few as half units (the kernel instantiation that
+    carries both kinds of item). Rows of every head are checked, with all
+    256 rows of the first query block of the last 8 heads, where the last
+    units (heaviest-first order within groups of 16 heads) fall."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    N = 1024
+    nqb = N // 256
+    H = (sms + 8 + nqb - 1) // nqb  # units = H * nqb: one wave plus a few
+    r = (H * nqb) % sms
+    assert 0 < r <= sms // 2
+    x = fin.make_inputs(fin.custom(1, H, N, d, False, seed=8100 + d))
+    o, lse = run_gpu(x)
+    g = np.random.Generator(np.random.PCG64(8200 + d))
+    rows = [h * N + g.choice(N, 32, replace=False) for h in range(H)]
+    rows += [h * N + np.arange(256) for h in range(max(0, H - 8), H)]
+    rows = np.unique(np.concatenate(rows))
+    o_ref, lse_ref = oracle_rows(oracle_mod, x, rows, False, x.workload.scale)
+    st = compare(o_to_numpy(o).reshape(-1, d)[rows], lse.cpu().numpy().reshape(-1)[rows], o_ref, lse_ref,
+                 f"whole+half d={d}", keys=visible_keys(N, False, rows % N))
+    assert_within(st)
