@@ -153,6 +153,15 @@ def fa_selftest_ex2_rate(cycles: int, sink: int, blocks: int, iters: int, stream
     return load_library().fa_selftest_ex2_rate(cycles, sink, blocks, iters, stream or None)
 
 
+def _current_stream_handle(torch, device) -> int:
+    """The raw cudaStream_t of the current stream on `device` (without
+    building a Stream object when torch offers the raw handle)."""
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(device.index if device.index is not None else torch.cuda.current_device())
+    return torch.cuda.current_stream(device).cuda_stream
+
+
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
                       return_lse: bool = True, stream=None):
     """O (bf16) and LSE (fp32) for bf16 CUDA tensors q, k, v of shape [B, H, N, d].
@@ -176,10 +185,10 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
         out = torch.empty_like(q)
     if return_lse and lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale), causal,
-                s.cuda_stream)
+    sp = stream.cuda_stream if stream is not None else _current_stream_handle(torch, q.device)
+    rc = (_lib or load_library()).fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                         lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale),
+                                         1 if causal else 0, sp or None)
     if rc != FA_OK:
         raise FaError(rc)
     return (out, lse) if return_lse else out
