@@ -223,11 +223,11 @@ def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: 
         out = torch.empty_like(q)
     if return_lse and lse is None:
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
-    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    sp = stream.cuda_stream if stream is not None else _current_stream_handle(torch, q.device)
     rc = fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                        lse.data_ptr() if lse is not None else None, cu_seqlens_q.data_ptr(),
                        cu_seqlens_k.data_ptr(), B, H, total_q, total_k, int(max_seqlen_q), d, float(scale),
-                       causal, s.cuda_stream)
+                       causal, sp)
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_varlen")
     return (out, lse) if return_lse else out
@@ -281,10 +281,10 @@ def attention_forward_heads(q, k, v, head_start: int, head_count: int, causal: b
     if head_count == 0:
         return out, lse
     eo, el = N * d * q.element_size(), N * 4   # bytes per head of q/k/v/out and of lse
-    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    sp = stream.cuda_stream if stream is not None else _current_stream_handle(torch, q.device)
     rc = fa_fwd(q.data_ptr() + head_start * eo, k.data_ptr() + head_start * eo, v.data_ptr() + head_start * eo,
                 out.data_ptr() + head_start * eo, lse.data_ptr() + head_start * el, 1, head_count, N, d,
-                float(scale), causal, s.cuda_stream)
+                float(scale), causal, sp)
     if rc != FA_OK:
         raise FaError(rc)
     return out, lse
