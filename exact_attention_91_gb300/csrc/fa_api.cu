@@ -567,11 +567,12 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
     if (rc != FA_OK) return rc;
     if (total_q == 0 || max_seqlen_q == 0) return FA_OK;  // no query: nothing to write
 
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     // a map needs at least one row: an empty key set is read through a one-row view of q
     if (encode_map_tokens(&tq, q, total_q, H, d) != FA_OK ||
         encode_map_tokens(&tk, total_k ? k : q, total_k ? total_k : 1, H, d) != FA_OK ||
-        encode_map_tokens(&tv, total_k ? v : q, total_k ? total_k : 1, H, d) != FA_OK)
+        encode_map_tokens(&tv, total_k ? v : q, total_k ? total_k : 1, H, d) != FA_OK ||
+        encode_map_tokens(&to, o, total_q, H, d) != FA_OK)
         return FA_ERR_LAUNCH;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -598,7 +599,7 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
     prm.n_full = prm.n_items;
     // a cluster split, or no more items than SMs: one item per CTA, no work queue
     prm.sched = (prm.nsplit > 1 || prm.n_items <= sms) ? nullptr : take_sched_slot(*st, captured);
-    return launch_any<true, false>(d, causal != 0, tq, tk, tv, tq, prm, sms, s);
+    return launch_any<true, false>(d, causal != 0, tq, tk, tv, to, prm, sms, s);
 }
 
 }  // extern "C"

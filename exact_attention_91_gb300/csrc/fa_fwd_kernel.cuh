@@ -856,7 +856,28 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap& tm_o, const FwdP
 #pragma unroll
                 for (int e = 0; e < 64; ++e) f[e] *= inv_l;
             };
-            if (p.nsplit == 1) {
+            if (p.nsplit == 1 && qr + kBlockM <= w.nq && w.tq0 + qr >= 0 && w.tq0 + qr + kBlockM <= p.total_q) {
+                // a tile wholly inside its sequence: staging box and one TMA
+                // store per 64-column box (tm_o is the (d, H, total) view of O)
+#pragma unroll
+                for (int b = 0; b < D / kBoxCols; ++b) {
+                    float o[64];
+                    row_box(b, o);
+                    if (row == 0) ptx::bulk_wait_group_read0();  // the box's previous store has read it
+                    ptx::named_bar_sync(1 + t, 128);
+                    pack_row64(o, [&](int q8, uint4 v) {
+                        *reinterpret_cast<uint4*>(stage + sw128_offset(row, q8)) = v;
+                    });
+                    ptx::fence_proxy_async_smem();
+                    ptx::named_bar_sync(1 + t, 128);
+                    if (row == 0) {
+                        ptx::tma_store_3d(&tm_o, stage_s, b * kBoxCols, w.head, w.tq0 + qr);
+                        ptx::bulk_commit_group();
+                    }
+                }
+                if (p.lse != nullptr && row_in)
+                    p.lse[static_cast<size_t>(w.head) * p.total_q + w.tq0 + q] = lse2 * 0.69314718055994531f;
+            } else if (p.nsplit == 1) {
                 // 16-byte row stores: a TMA box would run into the next sequence
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
                                                       (static_cast<size_t>(w.tq0 + q) * p.heads + w.head) * D);
@@ -963,8 +984,10 @@ __device__ __forceinline__ void cluster_merge(const FwdParams& p, int warp, int 
 }
 
 // The forward kernel. Equal length: tm_q/k/v/o are (d, N, B*H) views of
-// [B, H, N, d]. Variable length: tm_q/k/v are (d, H, total) views of
-// [total, H, d] and tm_o is unused (O is written with plain stores).
+// [B, H, N, d]. Variable length: tm_q/k/v/o are (d, H, total) views of
+// [total, H, d]; a query tile wholly inside its sequence is stored through
+// tm_o, a ragged last tile with plain row stores (a box would run into the
+// next sequence).
 template <int D, bool CAUSAL, bool VARLEN, bool HALF>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
